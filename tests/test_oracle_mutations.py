@@ -1,0 +1,73 @@
+"""Mutation smoke for the oracle pins: a mistake planted in the oracle (on the CPU)
+must make at least one pin fail.  Mirrors the mutation testing described in MSLK
+PR #393's test plan (an injected backward error must fail the suite)."""
+
+import numpy as np
+import pytest
+
+import oracle.dequant as D
+import oracle.formats as F
+import oracle.gemm as Gm
+import tests.test_oracle_dequant as TD
+import tests.test_oracle_formats as TF
+import tests.test_oracle_gemm as TG
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except (AssertionError, ValueError, IndexError):
+        return True
+    return False
+
+
+def test_swapped_nibbles_are_caught(monkeypatch):
+    def swapped(packed, cols):
+        packed = np.asarray(packed, dtype=np.uint8)
+        codes = np.empty(packed.shape[:-1] + (cols,), dtype=np.uint8)
+        codes[..., 0::2] = packed >> 4
+        codes[..., 1::2] = packed & 0x0F
+        return codes
+    monkeypatch.setattr(D, "unpack_fp4", swapped)
+    assert _fails(TD.test_fp4_nibble_order)
+    assert _fails(TD.test_mxfp4_against_torch, "random")
+
+
+def test_wrong_fp8_block_is_caught(monkeypatch):
+    monkeypatch.setattr(D, "FP8_BLOCK", 64)
+    assert _fails(TD.test_fp8_linear_example_shape_from_page)
+
+
+def test_wrong_mx_block_is_caught(monkeypatch):
+    monkeypatch.setattr(D, "MX_BLOCK", 16)
+    assert _fails(TD.test_scale_block_indexing_mxfp4_and_nvfp4)
+
+
+def test_skipped_scale_rounding_is_caught(monkeypatch):
+    real = D.bf16_round
+    calls = {"n": 0}
+
+    def skip_second(x):           # drops the BF16 cast of the scale (second call per dequant)
+        calls["n"] += 1
+        return np.asarray(x, dtype=np.float64) if calls["n"] % 3 == 1 else real(x)
+    monkeypatch.setattr(D, "bf16_round", skip_second)
+    assert _fails(TD.test_fp8_all_codes_ragged_shapes, 200, 300)
+
+
+def test_e4m3_bias_error_is_caught(monkeypatch):
+    monkeypatch.setattr(F, "E4M3_TABLE", F.E4M3_TABLE * 2.0)
+    assert _fails(TF.test_e4m3_table_matches_torch_float8)
+
+
+def test_transposed_wgrad_is_caught(monkeypatch):
+    monkeypatch.setattr(Gm, "wgrad", lambda g, x: Gm.as_f64(x).T @ Gm.as_f64(g))
+    assert _fails(TG.test_dgrad_wgrad_brute_force, 3)
+
+
+def test_grouped_off_by_one_is_caught(monkeypatch):
+    def shifted(offsets, e):
+        offsets = np.asarray(offsets, dtype=np.int64)
+        r0 = 0 if e == 0 else int(offsets[e - 1]) + 1
+        return r0, int(offsets[e])
+    monkeypatch.setattr(Gm, "expert_rows", shifted)
+    assert _fails(TG.test_grouped_dgrad_equals_block_diagonal_dense)
