@@ -162,3 +162,16 @@ def test_tolerance_check_catches_planted_errors():
     assert not Gm.check(a @ b[:, ::-1], ref, bound)[0]   # permuted output columns
     assert not Gm.check(np.zeros_like(ref), np.zeros_like(ref) + 1, 0.0)[0]
     assert Gm.check(np.zeros((2, 2)), np.zeros((2, 2)), 0.0)[0]
+
+
+def test_output_rounding_allowance_is_half_an_ulp():
+    # one-term products: the only error a correct BF16 result can have is its own rounding
+    rng = np.random.default_rng(8)
+    from oracle.formats import bf16_round
+    a = bf16_round(rng.standard_normal((50, 1)) * 3)
+    b = bf16_round(rng.standard_normal((1, 60)) * 3)
+    ref = a @ b
+    out = bf16_round(ref)
+    assert Gm.check(out, ref, Gm.tolerance(1, a, b))[0]
+    worse = out + np.sign(ref) * np.abs(ref) * 2.0 ** -7      # a full extra ulp-sized error
+    assert not Gm.check(worse, ref, 0.0)[0]
