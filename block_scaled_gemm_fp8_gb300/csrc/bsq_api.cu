@@ -1,0 +1,275 @@
+// bsq_api.cu -- the C entry points declared in include/bsq.h: host-side argument
+// validation, status codes, the per-device error word, and dispatch to the kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "bsq_internal.h"
+#include "../../include/bsq.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+// Per-device error word written by the kernels (BSQ_DEVERR_*); read and cleared by
+// bsq_get_device_error.  One int per device, allocated with the module.
+__device__ int32_t g_device_error;
+
+constexpr int kMaxDevices = 64;
+int32_t* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+bsq_status fail(bsq_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+bsq_status fail(bsq_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+// Device-specific set-up, done once per device with that device current.
+bsq_status device_state(int32_t** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(BSQ_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(BSQ_ERR_UNSUPPORTED, "libbsq is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    g_err_ptr[dev] = static_cast<int32_t*>(p);
+    g_num_sms[dev] = n;
+  }
+  *err = g_err_ptr[dev];
+  *sms = g_num_sms[dev];
+  return BSQ_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared validation of a packed operand [batch][rows][cols].
+bsq_status check_packed(const char* what, int32_t fmt, const void* data, const void* scale, const float* ts,
+                        int64_t batch, int64_t rows, int64_t cols, bool allow_bf16) {
+  if (fmt < BSQ_BF16 || fmt > BSQ_NVFP4) return fail(BSQ_ERR_INVALID_ARG, "%s: unknown format %d", what, fmt);
+  if (fmt == BSQ_BF16 && !allow_bf16) return fail(BSQ_ERR_UNSUPPORTED, "%s: BF16 is not a packed format here", what);
+  if (batch < 0 || rows < 0 || cols < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
+  const int64_t elems = batch * rows * cols;
+  if (elems > 0 && !data) return fail(BSQ_ERR_INVALID_ARG, "%s: null data", what);
+  if (elems > 0 && !aligned16(data)) return fail(BSQ_ERR_INVALID_ARG, "%s: data not 16-byte aligned", what);
+  if (fmt != BSQ_BF16 && elems > 0 && !scale) return fail(BSQ_ERR_INVALID_ARG, "%s: null scale", what);
+  if (fmt == BSQ_NVFP4 && elems > 0 && !ts) return fail(BSQ_ERR_INVALID_ARG, "%s: null tensor_scale", what);
+  if (fmt == BSQ_FP8_E4M3_B128 && elems > 0 && !aligned16(scale))
+    return fail(BSQ_ERR_INVALID_ARG, "%s: scale_inv not 16-byte aligned", what);
+  switch (fmt) {
+    case BSQ_BF16:
+      if (cols % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: BF16 cols %% 8 != 0 (row pitch must be 16 bytes)", what);
+      break;
+    case BSQ_FP8_E4M3_B128:
+      if (cols % 16) return fail(BSQ_ERR_UNSUPPORTED, "%s: FP8 cols %% 16 != 0 (row pitch must be 16 bytes)", what);
+      break;
+    case BSQ_MXFP4:
+      if (cols % 32) return fail(BSQ_ERR_INVALID_ARG, "%s: MXFP4 cols %% 32 != 0", what);
+      break;
+    case BSQ_NVFP4:
+      if (cols % 16) return fail(BSQ_ERR_INVALID_ARG, "%s: NVFP4 cols %% 16 != 0", what);
+      break;
+  }
+  if (rows > INT32_MAX || cols > INT32_MAX || batch > INT32_MAX)
+    return fail(BSQ_ERR_UNSUPPORTED, "%s: dimension above 2^31-1", what);
+  return BSQ_OK;
+}
+
+bsq_status check_gemm_common(const char* what, const void* g, int64_t S, int64_t N, int32_t fmt, int64_t K,
+                             const void* out) {
+  if (S < 0 || N < 0 || K < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
+  if (S > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(BSQ_ERR_UNSUPPORTED, "%s: size above 2^31-1", what);
+  if (S * N > 0 && (!g || !aligned16(g))) return fail(BSQ_ERR_INVALID_ARG, "%s: grad_out null or not 16-byte aligned", what);
+  if (N % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: N %% 8 != 0 (grad_out row pitch must be 16 bytes)", what);
+  if (fmt == BSQ_NVFP4 && K % 32)
+    return fail(BSQ_ERR_UNSUPPORTED, "%s: NVFP4 K %% 32 != 0 (packed row pitch must be 16 bytes)", what);
+  if (!out) return fail(BSQ_ERR_INVALID_ARG, "%s: null output", what);
+  if (!aligned16(out)) return fail(BSQ_ERR_INVALID_ARG, "%s: output not 16-byte aligned", what);
+  return BSQ_OK;
+}
+
+bsq_status run_gemm(bsq::GemmArgs& a, const char* what) {
+  int32_t* err = nullptr;
+  int sms = 0;
+  bsq_status st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  a.err = err;
+  a.num_sms = sms;
+  const char* msg = "";
+  if (bsq::launch_gemm(a, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
+  return BSQ_OK;
+}
+
+bsq_status zero_output(void* out, int64_t bytes, cudaStream_t s, const char* what) {
+  if (bytes <= 0) return BSQ_OK;
+  const cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(bytes), s);
+  if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return BSQ_OK;
+}
+
+}  // namespace
+
+namespace bsq {
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("BSQ_WAIT_LIMIT_MS");
+    const long ms = s ? std::atol(s) : 0;
+    return static_cast<uint64_t>(ms > 0 ? ms : 2000) * 1000000ull;
+  }();
+  return v;
+}
+}  // namespace bsq
+
+extern "C" {
+
+const char* bsq_status_string(int32_t s) {
+  switch (s) {
+    case BSQ_OK: return "BSQ_OK";
+    case BSQ_ERR_INVALID_ARG: return "BSQ_ERR_INVALID_ARG";
+    case BSQ_ERR_UNSUPPORTED: return "BSQ_ERR_UNSUPPORTED";
+    case BSQ_ERR_CUDA: return "BSQ_ERR_CUDA";
+    case BSQ_ERR_TIMEOUT: return "BSQ_ERR_TIMEOUT";
+    default: return "BSQ_ERR_UNKNOWN";
+  }
+}
+
+const char* bsq_last_error(void) { return g_msg; }
+
+int32_t bsq_num_sms(void) {
+  int32_t* err = nullptr;
+  int sms = 0;
+  return device_state(&err, &sms) == BSQ_OK ? sms : 0;
+}
+
+bsq_status bsq_get_device_error(int32_t* code, void* stream) {
+  if (!code) return fail(BSQ_ERR_INVALID_ARG, "bsq_get_device_error: null code");
+  int32_t* err = nullptr;
+  int sms = 0;
+  bsq_status st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "bsq_get_device_error: %s", cudaGetErrorString(e));
+  int32_t v = 0;
+  e = cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "bsq_get_device_error: %s", cudaGetErrorString(e));
+  const int32_t zero = 0;
+  e = cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "bsq_get_device_error: %s", cudaGetErrorString(e));
+  *code = v;
+  if (v == BSQ_DEVERR_TIMEOUT) return fail(BSQ_ERR_TIMEOUT, "a kernel wait ran out of time");
+  if (v == BSQ_DEVERR_BAD_OFFSETS) return fail(BSQ_ERR_INVALID_ARG, "offsets were not non-decreasing within [0, S]");
+  return BSQ_OK;
+}
+
+bsq_status bsq_dequant(int32_t fmt, const void* data, const void* scale, const float* tensor_scale, int64_t batch,
+                       int64_t rows, int64_t cols, void* out, void* stream) {
+  bsq_status st = check_packed("bsq_dequant", fmt, data, scale, tensor_scale, batch, rows, cols, false);
+  if (st != BSQ_OK) return st;
+  if (batch * rows * cols == 0) return BSQ_OK;
+  if (!out || !aligned16(out)) return fail(BSQ_ERR_INVALID_ARG, "bsq_dequant: output null or not 16-byte aligned");
+  if (fmt == BSQ_MXFP4 && !aligned16(data)) return fail(BSQ_ERR_INVALID_ARG, "bsq_dequant: data alignment");
+  int32_t* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  bsq::DequantArgs a{fmt, data, scale, tensor_scale, batch, rows, cols, out, sms, static_cast<cudaStream_t>(stream)};
+  const char* msg = "";
+  if (bsq::launch_dequant(a, &msg) != 0) return fail(BSQ_ERR_CUDA, "bsq_dequant: %s", msg);
+  return BSQ_OK;
+}
+
+bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
+                            const void* w_scale, const float* w_tensor_scale, int64_t K, void* grad_x,
+                            void* stream) {
+  const char* what = "bsq_linear_dgrad";
+  bsq_status st = check_gemm_common(what, grad_out, M, N, w_fmt, K, grad_x);
+  if (st != BSQ_OK) return st;
+  st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, true);
+  if (st != BSQ_OK) return st;
+  if (M == 0 || K == 0) return BSQ_OK;
+  if (N == 0) return zero_output(grad_x, M * K * 2, static_cast<cudaStream_t>(stream), what);
+  bsq::GemmArgs a{};
+  a.op = bsq::kDgrad; a.fmt = w_fmt; a.p_data = w_data; a.p_scale = w_scale; a.p_tensor_scale = w_tensor_scale;
+  a.p_batch = 1; a.p_rows = N; a.kc = K; a.g = grad_out; a.S = M; a.N = N; a.offsets = nullptr; a.E = 1;
+  a.out = grad_x; a.stream = static_cast<cudaStream_t>(stream);
+  return run_gemm(a, what);
+}
+
+bsq_status bsq_linear_wgrad(const void* grad_out, int64_t M, int64_t N, int32_t x_fmt, const void* x_data,
+                            const void* x_scale, const float* x_tensor_scale, int64_t K, void* grad_w,
+                            void* stream) {
+  const char* what = "bsq_linear_wgrad";
+  bsq_status st = check_gemm_common(what, grad_out, M, N, x_fmt, K, grad_w);
+  if (st != BSQ_OK) return st;
+  st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, true);
+  if (st != BSQ_OK) return st;
+  if (N == 0 || K == 0) return BSQ_OK;
+  if (M == 0) return zero_output(grad_w, N * K * 2, static_cast<cudaStream_t>(stream), what);
+  bsq::GemmArgs a{};
+  a.op = bsq::kWgrad; a.fmt = x_fmt; a.p_data = x_data; a.p_scale = x_scale; a.p_tensor_scale = x_tensor_scale;
+  a.p_batch = 1; a.p_rows = M; a.kc = K; a.g = grad_out; a.S = M; a.N = N; a.offsets = nullptr; a.E = 1;
+  a.out = grad_w; a.stream = static_cast<cudaStream_t>(stream);
+  return run_gemm(a, what);
+}
+
+bsq_status bsq_grouped_dgrad(const void* grad_out, int64_t S, int64_t N, int32_t w_fmt, const void* w_data,
+                             const void* w_scale, const float* w_tensor_scale, int64_t E, int64_t K,
+                             const int32_t* offsets, void* grad_x, void* stream) {
+  const char* what = "bsq_grouped_dgrad";
+  bsq_status st = check_gemm_common(what, grad_out, S, N, w_fmt, K, grad_x);
+  if (st != BSQ_OK) return st;
+  if (E < 1) return fail(BSQ_ERR_INVALID_ARG, "%s: E must be >= 1", what);
+  if (E > bsq::kMaxExperts) return fail(BSQ_ERR_UNSUPPORTED, "%s: E > %d", what, bsq::kMaxExperts);
+  if (!offsets) return fail(BSQ_ERR_INVALID_ARG, "%s: null offsets", what);
+  st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, E, N, K, true);
+  if (st != BSQ_OK) return st;
+  if (S == 0 || K == 0) return BSQ_OK;
+  if (N == 0) return fail(BSQ_ERR_UNSUPPORTED, "%s: N == 0 with S > 0 (rows to zero depend on offsets)", what);
+  bsq::GemmArgs a{};
+  a.op = bsq::kDgrad; a.fmt = w_fmt; a.p_data = w_data; a.p_scale = w_scale; a.p_tensor_scale = w_tensor_scale;
+  a.p_batch = E; a.p_rows = N; a.kc = K; a.g = grad_out; a.S = S; a.N = N; a.offsets = offsets; a.E = E;
+  a.out = grad_x; a.stream = static_cast<cudaStream_t>(stream);
+  return run_gemm(a, what);
+}
+
+bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N, int32_t x_fmt, const void* x_data,
+                             const void* x_scale, const float* x_tensor_scale, int64_t K, const int32_t* offsets,
+                             int64_t E, void* grad_w, void* stream) {
+  const char* what = "bsq_grouped_wgrad";
+  bsq_status st = check_gemm_common(what, grad_out, S, N, x_fmt, K, grad_w);
+  if (st != BSQ_OK) return st;
+  if (E < 1) return fail(BSQ_ERR_INVALID_ARG, "%s: E must be >= 1", what);
+  if (E > bsq::kMaxExperts) return fail(BSQ_ERR_UNSUPPORTED, "%s: E > %d", what, bsq::kMaxExperts);
+  if (!offsets) return fail(BSQ_ERR_INVALID_ARG, "%s: null offsets", what);
+  st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, S, K, true);
+  if (st != BSQ_OK) return st;
+  if (N == 0 || K == 0) return BSQ_OK;
+  if (S == 0) return zero_output(grad_w, E * N * K * 2, static_cast<cudaStream_t>(stream), what);
+  bsq::GemmArgs a{};
+  a.op = bsq::kWgrad; a.fmt = x_fmt; a.p_data = x_data; a.p_scale = x_scale; a.p_tensor_scale = x_tensor_scale;
+  a.p_batch = 1; a.p_rows = S; a.kc = K; a.g = grad_out; a.S = S; a.N = N; a.offsets = offsets; a.E = E;
+  a.out = grad_w; a.stream = static_cast<cudaStream_t>(stream);
+  return run_gemm(a, what);
+}
+
+}  // extern "C"

@@ -1,0 +1,599 @@
+// bsq_gemm.cu -- fused dequantize + BF16 tensor-core GEMM for the backward pass of a
+// block-scaled linear layer and of its grouped (mixture-of-experts) form.
+//
+//   dgrad  grad_X[S,K]   = grad_out[S,N]   @ deq(W[e])[N,K]     per expert rows
+//   wgrad  grad_W[e][N,K] = grad_out[r,N]^T @ deq(X)[r,K]        r = the expert's rows
+// (MSLK PR #393 "Implementation Method"; transformers PR #50031
+//  `FP8LinearFunction.backward`, `FP8GroupedMatmulFunction.backward`.)
+//
+// Both products are computed transposed, with the dequantized operand on the M side:
+//   D[m = column of the packed operand, n] = sum_k deq(P)[k, m] * G-side[k, n]
+// where P is W[e] (k = N index, n = token) for dgrad and X (k = token, n = N index)
+// for wgrad.  The packed operand is row-major with m contiguous, so it is an
+// "MN-major" A operand: no transpose kernel is needed on either side, and the
+// dequantization work per tensor-core FLOP is that of a 128-row operand.
+//
+// One persistent CTA per SM, 16 warps:
+//   warp 0      TMA producer: packed tile (or BF16 tile) + grad_out boxes per stage
+//   warp 1      MMA issuer (one thread): tcgen05.mma 128 x N x 16, FP32 accumulators in TMEM
+//   warp 2      TMEM allocation / release
+//   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
+//   warps 8-15  dequantization: packed codes (smem) -> BF16, written in the 128-byte
+//               swizzled MN-major layout the tensor core reads; also zero the rows of a
+//               k-block that lie outside the current expert (wgrad)
+// Stage hand-off: full[s] (TMA bytes landed) -> ready[s] (dequant done) -> empty[s]
+// (MMA done, tcgen05.commit).  Two TMEM accumulators (2 x 256 columns) let the
+// epilogue of one tile overlap the main loop of the next.  Tiles are walked in a
+// static persistent order; the expert of a tile comes from a per-CTA prefix sum of
+// tile counts over the offsets.  Every wait is bounded by %globaltimer and records a
+// timeout in the device error word instead of hanging.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "bsq_decode.cuh"
+#include "bsq_internal.h"
+#include "bsq_ptx.cuh"
+#include "../../include/bsq.h"
+
+namespace bsq {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kBoxBytes = 64 * 64 * 2;          // one 64x64 BF16 box = one swizzle column of 64 rows
+constexpr int kABytes = kTileM * kTileK * 2;     // 16 KB: dequantized operand, 2 swizzle columns
+constexpr int kBBytes = kTileN * kTileK * 2;     // 32 KB: grad_out side, 4 boxes
+constexpr int kTmemCols = 512;                   // 2 accumulators x 256 FP32 columns
+
+template <int FMT>
+struct Fmt {
+  static constexpr int kPBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileK * kTileM : (FMT == BSQ_BF16 ? 0 : kTileK * kTileM / 2);
+  static constexpr int kPRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileM : kTileM / 2;
+  static constexpr int kStages = FMT == BSQ_FP8_E4M3_B128 ? 3 : 4;
+  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
+};
+
+struct Params {
+  const uint8_t* scale;
+  const float* tensor_scale;
+  const int32_t* offsets;
+  __nv_bfloat16* out;
+  int32_t* err;
+  int64_t out_expert_stride;  // wgrad: N*K; dgrad: 0
+  int64_t p_rows;             // packed rows per batch entry
+  int32_t E;
+  int32_t S;
+  int32_t N;
+  int32_t Kc;
+  int32_t num_m;              // ceil(Kc / 128)
+  int32_t scale_ld;           // scale row pitch (elements)
+  int32_t scale_rblocks;      // FP8: ceil(p_rows / 128)
+  uint64_t timeout_ns;
+};
+
+struct SharedTail {
+  uint64_t full[4];
+  uint64_t ready[4];
+  uint64_t empty[4];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+  int32_t total_tiles;
+  int32_t pad;
+  int32_t off[kMaxExperts + 1];  // off[e] = first row of expert e, off[E] = end
+  int32_t pre[kMaxExperts + 1];  // prefix of tile counts
+};
+
+__device__ __forceinline__ void record_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
+
+// Bounded wait on an mbarrier phase; false when the CTA aborted or the limit ran out.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                        int32_t* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1u;
+      record_error(err, BSQ_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+struct TileInfo {
+  int e, mt, nt, n_valid, kblocks, r0, r1;
+};
+
+template <int OP>
+__device__ __forceinline__ TileInfo decode_tile(int t, int& e_cur, const SharedTail& sh, const Params& p) {
+  while (sh.pre[e_cur + 1] <= t) ++e_cur;
+  TileInfo ti;
+  const int local = t - sh.pre[e_cur];
+  ti.e = e_cur;
+  ti.mt = local % p.num_m;
+  ti.nt = local / p.num_m;
+  ti.r0 = sh.off[e_cur];
+  ti.r1 = sh.off[e_cur + 1];
+  const int cnt = ti.r1 - ti.r0;
+  if (OP == kDgrad) {
+    ti.n_valid = min(kTileN, cnt - ti.nt * kTileN);
+    ti.kblocks = (p.N + kTileK - 1) / kTileK;
+  } else {
+    ti.n_valid = min(kTileN, p.N - ti.nt * kTileN);
+    ti.kblocks = (cnt + kTileK - 1) / kTileK;
+  }
+  return ti;
+}
+
+template <int FMT>
+__device__ __forceinline__ int lane_to_col(int i) {
+  if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) return (i & ~7) | perm_fp4(i & 7);
+  if (FMT == BSQ_FP8_E4M3_B128) return (i & ~7) | perm_fp8(i & 7);
+  return i;
+}
+
+template <int FMT, int OP>
+__global__ void __launch_bounds__(kThreads, 1)
+    bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_g,
+                    const Params p) {
+  using F = Fmt<FMT>;
+  constexpr int kStages = F::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SharedTail& sh = *reinterpret_cast<SharedTail*>(smem + kStages * F::kStageBytes);
+  volatile uint32_t* abort_flag = &sh.abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  auto stage_a = [&](int s) { return smem + s * F::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + s * F::kStageBytes + kABytes; };
+  auto stage_p = [&](int s) { return smem + s * F::kStageBytes + kABytes + kBBytes; };
+
+  // ---------------------------------------------------------------- set-up
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.ready[s]), 8);
+      mbar_init(smem_u32(&sh.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh.tmem_full[b]), 1);
+      mbar_init(smem_u32(&sh.tmem_empty[b]), 4);
+    }
+    mbar_init(smem_u32(&sh.drain), 1);
+    sh.abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_p);
+    tma_prefetch_map(&tm_g);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  // Expert table: off[e] = start row of expert e.  A null offsets pointer is one group.
+  const int E = p.E;
+  for (int e = tid; e <= E; e += kThreads) {
+    int v;
+    if (e == 0) v = 0;
+    else v = p.offsets ? __ldg(p.offsets + (e - 1)) : p.S;
+    sh.off[e] = v;
+  }
+  __syncthreads();
+  if (warp == 3) {
+    // Validate and prefix-sum the tile counts: lane l owns experts [l*per, (l+1)*per).
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int bad = 0, sum = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int a = sh.off[e], b = sh.off[e + 1];
+      if (b < a || b > p.S || a < 0) bad = 1;
+      const int cnt = max(b - a, 0);
+      const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
+      sum += ntiles * p.num_m;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    int run = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      sh.pre[e] = run;
+      const int cnt = max(sh.off[e + 1] - sh.off[e], 0);
+      const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
+      run += ntiles * p.num_m;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      sh.pre[E] = total;
+      sh.total_tiles = bad ? 0 : total;
+      if (bad && blockIdx.x == 0) record_error(p.err, BSQ_DEVERR_BAD_OFFSETS);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh.tmem_base;
+  const int total_tiles = sh.total_tiles;
+  const uint64_t limit = p.timeout_ns;
+
+  // ---------------------------------------------------------------- roles
+  if (warp == 0) {
+    // ===== TMA producer =====
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int e_cur = 0;
+      uint32_t pend_mask = 0, pend_par = 0;  // stages with loads in flight (for an orderly abort)
+      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+        const int m0 = ti.mt * kTileM;
+        const int nbox = (ti.n_valid + 63) >> 6;
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, p.err, limit)) break;
+          const uint32_t full = smem_u32(&sh.full[stage]);
+          const uint32_t bytes = (FMT == BSQ_BF16 ? 2 * kBoxBytes : F::kPBytes) + nbox * kBoxBytes;
+          mbar_arrive_expect_tx(full, bytes);
+          pend_mask |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          const int prow = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
+          const int pbatch = OP == kDgrad ? ti.e : 0;
+          if (FMT == BSQ_BF16) {
+            tma_load_3d(smem_u32(stage_a(stage)), &tm_p, full, m0, prow, pbatch);
+            tma_load_3d(smem_u32(stage_a(stage) + kBoxBytes), &tm_p, full, m0 + 64, prow, pbatch);
+          } else {
+            const int x = FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2;
+            tma_load_3d(smem_u32(stage_p(stage)), &tm_p, full, x, prow, pbatch);
+          }
+          for (int j = 0; j < nbox; ++j) {
+            if (OP == kDgrad)
+              tma_load_2d(smem_u32(stage_b(stage) + j * kBoxBytes), &tm_g, full, kb * kTileK,
+                          ti.r0 + ti.nt * kTileN + 64 * j);
+            else
+              tma_load_2d(smem_u32(stage_b(stage) + j * kBoxBytes), &tm_g, full, ti.nt * kTileN + 64 * j,
+                          ti.r0 + kb * kTileK);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (*abort_flag) {
+        // Let every issued copy land before the CTA's shared memory is released.
+        for (int s = 0; s < kStages; ++s)
+          if (pend_mask & (1u << s)) {
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(smem_u32(&sh.full[s]), (pend_par >> s) & 1u) &&
+                   global_timer_ns() - t0 < limit) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ===== MMA issuer =====
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int e_cur = 0;
+      uint32_t acc = 0;
+      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+        if (ti.kblocks == 0) continue;
+        const uint32_t buf = acc & 1u;
+        const uint32_t acc_phase = (acc >> 1) & 1u;
+        if (!wait_phase(smem_u32(&sh.tmem_empty[buf]), acc_phase ^ 1u, abort_flag, p.err, limit)) break;
+        tc_fence_after();
+        const uint32_t n_mma = (static_cast<uint32_t>(ti.n_valid) + 15u) & ~15u;
+        const uint32_t idesc = idesc_bf16_f32(kTileM, n_mma, true, OP == kWgrad);
+        const uint32_t d_tmem = tmem_base + buf * kTileN;
+        bool ok = true;
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          if (!wait_phase(smem_u32(&sh.ready[stage]), phase, abort_flag, p.err, limit)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(stage_a(stage));
+          const uint32_t b_base = smem_u32(stage_b(stage));
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+            // A: MN-major, swizzle columns of 64 m at 8 KB, 8-row groups at 1 KB; 16 k-rows = 2 KB.
+            const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
+            uint64_t bdesc;
+            if (OP == kDgrad)  // B: K-major rows of 128 bytes (64 k), 8-row groups at 1 KB; 16 k = 32 B
+              bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            else               // B: MN-major like A
+              bdesc = sdesc_sw128(b_base + kk * 2048, kBoxBytes, 1024);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&sh.empty[stage]));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&sh.tmem_full[buf]));
+        ++acc;
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ===== epilogue =====
+    const int q = warp - 4;                  // TMEM lane quarter (warp % 4)
+    const int i = q * 32 + lane;             // accumulator row = tile m index (permuted)
+    const int mcol = lane_to_col<FMT>(i);
+    int e_cur = 0;
+    uint32_t acc = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+      const int m = ti.mt * kTileM + mcol;
+      const bool mok = m < p.Kc;
+      __nv_bfloat16* obase;
+      if (OP == kDgrad)
+        obase = p.out + static_cast<int64_t>(ti.r0 + ti.nt * kTileN) * p.Kc + m;
+      else
+        obase = p.out + ti.e * p.out_expert_stride + static_cast<int64_t>(ti.nt * kTileN) * p.Kc + m;
+      if (ti.kblocks == 0) {
+        // wgrad of an expert without rows: exact zeros
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+        if (mok)
+          for (int n = 0; n < ti.n_valid; ++n) obase[static_cast<int64_t>(n) * p.Kc] = z;
+        continue;
+      }
+      const uint32_t buf = acc & 1u;
+      const uint32_t acc_phase = (acc >> 1) & 1u;
+      ++acc;
+      bool ok = wait_phase(smem_u32(&sh.tmem_full[buf]), acc_phase, abort_flag, p.err, limit);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int nchunks = (ti.n_valid + 31) >> 5;
+      for (int c = 0; c < nchunks; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + c * 32, v);
+        tmem_wait_ld();
+        if (c == nchunks - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh.tmem_empty[buf]));
+        }
+        if (mok) {
+          const int nlim = min(32, ti.n_valid - c * 32);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nlim) obase[static_cast<int64_t>(c * 32 + j) * p.Kc] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ===== dequantization =====
+    const int dw = warp - 8;  // 0..7
+    int stage = 0;
+    uint32_t phase = 0;
+    int e_cur = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+      const int m0 = ti.mt * kTileM;
+      const int pbatch = OP == kDgrad ? ti.e : 0;
+      float tscale = 0.f;
+      if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + pbatch);
+      bool ok = true;
+      for (int kb = 0; kb < ti.kblocks; ++kb) {
+        // rows of this k-block that belong to the contraction
+        const int prow0 = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
+        const int kvalid = OP == kDgrad ? min(kTileK, p.N - kb * kTileK) : min(kTileK, ti.r1 - prow0);
+        // Scale bytes for this thread's 4 chunks, fetched before the wait.
+        uint32_t sraw[4];
+        float sf[4];
+        if (FMT != BSQ_BF16) {
+#pragma unroll
+          for (int ps = 0; ps < 4; ++ps) {
+            const int r = ps * 16 + dw * 2 + (lane >> 4);
+            const int col = m0 + 8 * (lane & 15);
+            sraw[ps] = 0;
+            sf[ps] = 0.f;
+            if (r < kvalid && col < p.Kc) {
+              const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + r;
+              if (FMT == BSQ_MXFP4)
+                sraw[ps] = __ldg(p.scale + grow * p.scale_ld + (col >> 5));
+              else if (FMT == BSQ_NVFP4)
+                sraw[ps] = __ldg(p.scale + grow * p.scale_ld + (col >> 4));
+              else
+                sf[ps] = __ldg(reinterpret_cast<const float*>(p.scale) +
+                               (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + r) >> 7)) * p.scale_ld +
+                               (col >> 7));
+            }
+          }
+        }
+        ok = wait_phase(smem_u32(&sh.full[stage]), phase, abort_flag, p.err, limit);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        uint8_t* a_tile = stage_a(stage);
+        if (FMT != BSQ_BF16) {
+          const uint8_t* p_tile = stage_p(stage);
+#pragma unroll
+          for (int ps = 0; ps < 4; ++ps) {
+            const int r = ps * 16 + dw * 2 + (lane >> 4);
+            const int c = lane & 15;
+            const bool valid = r < kvalid && (m0 + 8 * c) < p.Kc;
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (valid) {
+              if (FMT == BSQ_FP8_E4M3_B128) {
+                const uint2 w = *reinterpret_cast<const uint2*>(p_tile + r * F::kPRowBytes + c * 8);
+                const ScaleBf16 s = make_scale_fp8(sf[ps]);
+                decode_e4m3x4(w.x, s, o.x, o.y);
+                decode_e4m3x4(w.y, s, o.z, o.w);
+              } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(p_tile + r * F::kPRowBytes + c * 4);
+                const ScaleBf16 s = FMT == BSQ_MXFP4 ? make_scale_e8m0(sraw[ps]) : make_scale_nvfp4(sraw[ps], tscale);
+                uint32_t pr[4];
+                decode_e2m1x8(w, s, pr);
+                o = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+              }
+            }
+            const int atom = c >> 3, ch = c & 7;
+            *reinterpret_cast<uint4*>(a_tile + atom * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
+          }
+        } else if (kvalid < kTileK) {
+          // BF16 operand from TMA: zero the rows outside the contraction
+          for (int idx = dw * 32 + lane; idx < (kTileK - kvalid) * 16; idx += 256) {
+            const int r = kvalid + idx / 16, c = idx % 16;
+            *reinterpret_cast<uint4*>(a_tile + (c >> 3) * kBoxBytes + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (OP == kWgrad && kvalid < kTileK) {
+          // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must not
+          // reach the products: zero them in every loaded box.
+          uint8_t* b_tile = stage_b(stage);
+          const int nbox = (ti.n_valid + 63) >> 6;
+          for (int idx = dw * 32 + lane; idx < (kTileK - kvalid) * 8 * nbox; idx += 256) {
+            const int box = idx / ((kTileK - kvalid) * 8);
+            const int rem = idx % ((kTileK - kvalid) * 8);
+            const int r = kvalid + rem / 8, c = rem % 8;
+            *reinterpret_cast<uint4*>(b_tile + box * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.ready[stage]));
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == 1 && lane == 0) {
+    // Every MMA this thread issued has completed once the drain barrier fires.
+    umma_commit(smem_u32(&sh.drain));
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(smem_u32(&sh.drain), 0) && global_timer_ns() - t0 < limit) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* base, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const uint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int FMT, int OP>
+int launch_typed(const GemmArgs& a, const char** msg) {
+  using F = Fmt<FMT>;
+  CUtensorMap tm_p, tm_g;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.S)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {64, 64};
+    if (!encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B)) {
+      *msg = "tensor map encoding failed for grad_out";
+      return -1;
+    }
+  }
+  {
+    uint64_t row_bytes;
+    CUtensorMapDataType dt;
+    uint32_t box0;
+    CUtensorMapSwizzle sw;
+    uint64_t inner;
+    if (FMT == BSQ_BF16) {
+      dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; inner = a.kc; row_bytes = a.kc * 2; box0 = 64; sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    } else if (FMT == BSQ_FP8_E4M3_B128) {
+      dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; inner = a.kc; row_bytes = a.kc; box0 = kTileM; sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    } else {
+      dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; inner = a.kc / 2; row_bytes = a.kc / 2; box0 = kTileM / 2; sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    }
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(a.p_rows), static_cast<uint64_t>(a.p_batch)};
+    const uint64_t strides[2] = {row_bytes, row_bytes * static_cast<uint64_t>(a.p_rows)};
+    const uint32_t box[3] = {box0, static_cast<uint32_t>(kTileK), 1};
+    if (!encode_map(&tm_p, dt, 3, a.p_data, dims, strides, box, sw)) {
+      *msg = "tensor map encoding failed for the packed operand";
+      return -1;
+    }
+  }
+  Params p;
+  p.scale = static_cast<const uint8_t*>(a.p_scale);
+  p.tensor_scale = a.p_tensor_scale;
+  p.offsets = a.offsets;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.err = a.err;
+  p.out_expert_stride = OP == kWgrad ? a.N * a.kc : 0;
+  p.p_rows = a.p_rows;
+  p.E = static_cast<int32_t>(a.E);
+  p.S = static_cast<int32_t>(a.S);
+  p.N = static_cast<int32_t>(a.N);
+  p.Kc = static_cast<int32_t>(a.kc);
+  p.num_m = static_cast<int32_t>((a.kc + kTileM - 1) / kTileM);
+  p.scale_ld = FMT == BSQ_MXFP4 ? static_cast<int32_t>(a.kc / 32)
+               : FMT == BSQ_NVFP4 ? static_cast<int32_t>(a.kc / 16)
+                                  : static_cast<int32_t>((a.kc + 127) / 128);
+  p.scale_rblocks = static_cast<int32_t>((a.p_rows + 127) / 128);
+  p.timeout_ns = wait_limit_ns();
+
+  // Upper bound of the tile count (the exact count depends on the offsets, read on the device).
+  const int64_t nn = (a.N + kTileN - 1) / kTileN;
+  const int64_t bound = OP == kDgrad ? p.num_m * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_m * nn * a.E;
+  int64_t grid = bound < a.num_sms ? bound : a.num_sms;
+  if (grid < 1) grid = 1;
+  const size_t smem = static_cast<size_t>(F::kStages) * F::kStageBytes + sizeof(SharedTail) + 1024;
+  auto kern = bsq_gemm_kernel<FMT, OP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    kern<<<dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, a.stream>>>(tm_p, tm_g, p);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    *msg = cudaGetErrorString(e);
+    return static_cast<int>(e);
+  }
+  return 0;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmArgs& a, const char** msg) {
+#define BSQ_CASE(F_, O_) \
+  if (a.fmt == F_ && a.op == O_) return launch_typed<F_, O_>(a, msg);
+  BSQ_CASE(BSQ_BF16, kDgrad)
+  BSQ_CASE(BSQ_BF16, kWgrad)
+  BSQ_CASE(BSQ_FP8_E4M3_B128, kDgrad)
+  BSQ_CASE(BSQ_FP8_E4M3_B128, kWgrad)
+  BSQ_CASE(BSQ_MXFP4, kDgrad)
+  BSQ_CASE(BSQ_MXFP4, kWgrad)
+  BSQ_CASE(BSQ_NVFP4, kDgrad)
+  BSQ_CASE(BSQ_NVFP4, kWgrad)
+#undef BSQ_CASE
+  *msg = "unsupported format/op";
+  return -1;
+}
+
+}  // namespace bsq

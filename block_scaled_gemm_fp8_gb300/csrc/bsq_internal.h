@@ -1,0 +1,61 @@
+// bsq_internal.h -- launch descriptions shared between the host entry points (bsq_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsq {
+
+enum GemmOp : int { kDgrad = 0, kWgrad = 1 };
+
+// Fixed tile shape of the fused kernel (see bsq_gemm.cu):
+//   M side (tensor-memory lanes): 128 columns of the packed operand's contiguous axis
+//   N side: up to 256 tokens (dgrad) or grad_out columns (wgrad)
+//   K step: 64 rows of the packed operand per pipeline stage
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kTileK = 64;
+constexpr int kMaxExperts = 1024;
+
+struct GemmArgs {
+  int op;            // kDgrad / kWgrad
+  int fmt;           // bsq_format of the packed (dequantized) operand
+  const void* p_data;
+  const void* p_scale;
+  const float* p_tensor_scale;
+  int64_t p_batch;   // dgrad: E (weights per expert); wgrad: 1
+  int64_t p_rows;    // rows of one packed matrix (dgrad: N; wgrad: S)
+  int64_t kc;        // packed operand columns (K)
+  const void* g;     // grad_out bf16 [S][N]
+  int64_t S;
+  int64_t N;
+  const int32_t* offsets;  // device int32 [E] cumulative ends; nullptr = one group of S rows
+  int64_t E;
+  void* out;         // dgrad: bf16 [S][K]; wgrad: bf16 [E][N][K]
+  int32_t* err;      // device error word
+  int num_sms;
+  cudaStream_t stream;
+};
+
+// Returns a cudaError_t-style code (0 = launched) and fills `msg` on failure.
+int launch_gemm(const GemmArgs& a, const char** msg);
+
+struct DequantArgs {
+  int fmt;
+  const void* data;
+  const void* scale;
+  const float* tensor_scale;
+  int64_t batch, rows, cols;
+  void* out;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+int launch_dequant(const DequantArgs& a, const char** msg);
+
+// Wait limit of every pipeline wait inside the kernels (nanoseconds of %globaltimer).
+uint64_t wait_limit_ns();
+
+}  // namespace bsq

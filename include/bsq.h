@@ -1,0 +1,148 @@
+/*
+ * bsq.h -- C ABI of libbsq: the backward pass of block-scaled low-precision linear
+ * layers and of their grouped (mixture-of-experts) form, on one GB300 GPU (sm_103a).
+ *
+ * What is computed (the "dequantize, then BF16 matmul" backward):
+ *   MSLK PR #393 "Add Autograd Backward Support for FP4 GEMM Custom Ops",
+ *   section "Implementation Method": saved packed FP4 operands are dequantized to
+ *   BF16 and the standard gradients are taken,
+ *       grad_X = grad_out @ W_bf16        grad_W = grad_out^T @ X_bf16
+ *   transformers PR #50031 "Train adapters on top of FP8 weights":
+ *   `_dequantize_fp8_weight` (E4M3 weights, float32 scale_inv per 128x128 block,
+ *   scale cast to the gradient dtype), `FP8LinearFunction.backward` (dgrad only,
+ *   the FP8 weight is frozen) and `FP8GroupedMatmulFunction.backward` (grouped dgrad
+ *   over int32 expert offsets).
+ *
+ * Dequantization rule (bit-exact): out = RNE_bf16( bf16(code value) * RNE_bf16(scale) ).
+ *   FP8 E4M3      scale = scale_inv[b][r/128][c/128]                         (float32)
+ *   MXFP4         scale = 2^(e8m0[b][r][c/32] - 127), byte 255 = NaN
+ *   NVFP4         scale = RNE_fp32( e4m3[b][r][c/16] * tensor_scale[b] )
+ * FP4 packing: byte j of a row holds element 2j in bits 0-3 and 2j+1 in bits 4-7.
+ * The GEMMs accumulate in FP32 (tensor cores) and round the result once to BF16.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers except `code` in bsq_get_device_error are DEVICE pointers into
+ *     the current CUDA device's memory; the caller allocates and owns every buffer.
+ *     Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Tensors are dense and row-major: [batch][rows][cols], cols contiguous.
+ *   - Packed operand of format `fmt`:
+ *       BSQ_BF16           data bf16[batch][rows][cols]; scale, tensor_scale unused
+ *       BSQ_FP8_E4M3_B128  data u8  [batch][rows][cols];
+ *                          scale f32[batch][ceil(rows/128)][ceil(cols/128)]
+ *       BSQ_MXFP4          data u8  [batch][rows][cols/2]; scale u8 [batch][rows][cols/32]
+ *       BSQ_NVFP4          data u8  [batch][rows][cols/2]; scale u8 (E4M3) [batch][rows][cols/16];
+ *                          tensor_scale f32[batch]
+ *   - Alignment: data/scale base pointers 16-byte aligned; the row pitch of every
+ *     TMA-read tensor a multiple of 16 bytes, i.e. N % 8 == 0 for grad_out, and
+ *     K % 16 (FP8), K % 32 (MXFP4, NVFP4), K % 8 (BF16) for the packed operand.
+ *     M, S and the expert sizes are arbitrary.
+ *   - Errors: every call validates its arguments on the host first and returns a
+ *     status without launching anything when they are wrong.  Nothing is thrown.
+ *     BSQ_ERR_UNSUPPORTED marks a well-formed request the library does not serve
+ *     (an alignment above, too many experts); BSQ_ERR_CUDA a failed launch.
+ *     Device-side conditions (decreasing offsets, a pipeline wait that ran out of
+ *     time) are recorded in a per-device error word read by bsq_get_device_error.
+ *   - Allocation: the library allocates no device memory per call.
+ */
+#ifndef BSQ_H
+#define BSQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSQ_OK = 0,
+  BSQ_ERR_INVALID_ARG = 1,
+  BSQ_ERR_UNSUPPORTED = 2,
+  BSQ_ERR_CUDA = 3,
+  BSQ_ERR_TIMEOUT = 4
+} bsq_status;
+
+typedef enum {
+  BSQ_BF16 = 0,
+  BSQ_FP8_E4M3_B128 = 1,
+  BSQ_MXFP4 = 2,
+  BSQ_NVFP4 = 3
+} bsq_format;
+
+/* Device error word values (bsq_get_device_error). */
+#define BSQ_DEVERR_NONE 0
+#define BSQ_DEVERR_TIMEOUT 1      /* a pipeline wait exceeded its time limit; the kernel returned early */
+#define BSQ_DEVERR_BAD_OFFSETS 2  /* offsets decreasing, negative or beyond S; no output was written */
+
+/*
+ * bsq_dequant -- decode a packed operand to BF16 (the standalone dequantization the
+ * transformers PR #50031 `_dequantize_fp8_weight` performs; MSLK PR #393's FP4
+ * dequantization helpers).  out: bf16[batch][rows][cols].  fmt must not be BSQ_BF16.
+ * Requirements: cols % 16 == 0 (FP8), cols % 32 == 0 (MXFP4), cols % 16 == 0 (NVFP4).
+ */
+bsq_status bsq_dequant(int32_t fmt, const void* data, const void* scale, const float* tensor_scale,
+                       int64_t batch, int64_t rows, int64_t cols, void* out, void* stream);
+
+/*
+ * bsq_linear_dgrad -- grad_x[M][K] = grad_out[M][N] @ deq(W)[N][K]
+ * (MSLK PR #393, Implementation Method; transformers PR #50031 FP8LinearFunction.backward).
+ * grad_out: bf16[M][N]; W: packed [1][N][K] in w_fmt; grad_x: bf16[M][K] (fully written).
+ */
+bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N,
+                            int32_t w_fmt, const void* w_data, const void* w_scale,
+                            const float* w_tensor_scale, int64_t K, void* grad_x, void* stream);
+
+/*
+ * bsq_linear_wgrad -- grad_w[N][K] = grad_out[M][N]^T @ deq(X)[M][K]
+ * (MSLK PR #393, Implementation Method).  X: packed [1][M][K] in x_fmt (BSQ_BF16 allowed).
+ * grad_w: bf16[N][K] (fully written; M == 0 gives zeros).
+ */
+bsq_status bsq_linear_wgrad(const void* grad_out, int64_t M, int64_t N,
+                            int32_t x_fmt, const void* x_data, const void* x_scale,
+                            const float* x_tensor_scale, int64_t K, void* grad_w, void* stream);
+
+/*
+ * bsq_grouped_dgrad -- per expert e, grad_x[r0:r1] = grad_out[r0:r1] @ deq(W[e])
+ * (transformers PR #50031 FP8GroupedMatmulFunction.backward).
+ * offsets: device int32[E], cumulative END offsets without a leading zero
+ * (expert e owns rows [e ? offsets[e-1] : 0, offsets[e])), non-decreasing, offsets[E-1] <= S.
+ * W: packed [E][N][K]; w_tensor_scale (NVFP4) is per expert, f32[E].
+ * grad_x: bf16[S][K]; rows >= offsets[E-1] are neither read (grad_out) nor written.
+ * 1 <= E <= 1024.
+ */
+bsq_status bsq_grouped_dgrad(const void* grad_out, int64_t S, int64_t N,
+                             int32_t w_fmt, const void* w_data, const void* w_scale,
+                             const float* w_tensor_scale, int64_t E, int64_t K,
+                             const int32_t* offsets, void* grad_x, void* stream);
+
+/*
+ * bsq_grouped_wgrad -- per expert e, grad_w[e] = grad_out[r0:r1]^T @ deq(X)[r0:r1]
+ * (MSLK PR #393, Implementation Method, applied per group).  X: packed [1][S][K].
+ * grad_w: bf16[E][N][K], every expert written; an expert with no rows gets exact zeros.
+ * Rows >= offsets[E-1] of grad_out and X are never read.  1 <= E <= 1024.
+ */
+bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N,
+                             int32_t x_fmt, const void* x_data, const void* x_scale,
+                             const float* x_tensor_scale, int64_t K, const int32_t* offsets,
+                             int64_t E, void* grad_w, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* bsq_status_string(int32_t status);
+
+/* Message describing the last failing call on this host thread ("" if none). */
+const char* bsq_last_error(void);
+
+/*
+ * bsq_get_device_error -- synchronize `stream`, then read and clear the current
+ * device's error word into *code (host pointer).  Returns BSQ_ERR_TIMEOUT when the
+ * word held BSQ_DEVERR_TIMEOUT, BSQ_ERR_INVALID_ARG for BSQ_DEVERR_BAD_OFFSETS, else BSQ_OK.
+ */
+bsq_status bsq_get_device_error(int32_t* code, void* stream);
+
+/* Number of SMs the persistent kernels are sized for on the current device (0 on error). */
+int32_t bsq_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSQ_H */

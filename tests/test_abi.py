@@ -1,0 +1,71 @@
+"""The C ABI on the CPU: the library loads, exports every entry point include/bsq.h
+declares, and its host-side validation rejects bad arguments before touching a GPU
+(no compute call runs here)."""
+
+import ctypes
+import os
+
+import pytest
+
+from block_scaled_gemm_fp8_gb300 import bsq
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced by host validation
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(bsq.LIB_PATH):
+        from block_scaled_gemm_fp8_gb300 import build
+        build.build()
+    return bsq.lib()
+
+
+def test_exports_every_declared_entry_point(L):
+    names = bsq.header_entry_points()
+    assert set(names) >= {"bsq_dequant", "bsq_linear_dgrad", "bsq_linear_wgrad", "bsq_grouped_dgrad",
+                          "bsq_grouped_wgrad", "bsq_status_string", "bsq_get_device_error"}
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) <= set(bsq.SIGNATURES), "binding is missing a declared entry point"
+
+
+def test_status_strings(L):
+    assert bsq.status_string(0) == "BSQ_OK"
+    assert bsq.status_string(1) == "BSQ_ERR_INVALID_ARG"
+    assert bsq.status_string(4) == "BSQ_ERR_TIMEOUT"
+    assert bsq.status_string(99) == "BSQ_ERR_UNKNOWN"
+
+
+def _dgrad(L, g=FAKE, M=64, N=128, fmt=1, w=FAKE, s=FAKE, ts=None, K=256, out=FAKE):
+    return L.bsq_linear_dgrad(g, M, N, fmt, w, s, ts, K, out, None)
+
+
+def test_validation_rejects_bad_arguments(L):
+    assert _dgrad(L, g=None) == bsq.BSQ_ERR_INVALID_ARG
+    assert _dgrad(L, out=None) == bsq.BSQ_ERR_INVALID_ARG
+    assert _dgrad(L, out=FAKE + 8) == bsq.BSQ_ERR_INVALID_ARG        # misaligned
+    assert _dgrad(L, fmt=9) == bsq.BSQ_ERR_INVALID_ARG
+    assert _dgrad(L, M=-1) == bsq.BSQ_ERR_INVALID_ARG
+    assert _dgrad(L, N=12) == bsq.BSQ_ERR_UNSUPPORTED               # grad_out row pitch not 16 B
+    assert _dgrad(L, fmt=2, K=48) == bsq.BSQ_ERR_INVALID_ARG         # MXFP4 needs K % 32
+    assert _dgrad(L, fmt=3, K=48) == bsq.BSQ_ERR_UNSUPPORTED         # NVFP4 K % 32 for TMA pitch
+    assert _dgrad(L, fmt=3, ts=None) == bsq.BSQ_ERR_INVALID_ARG      # NVFP4 needs a tensor scale
+    assert _dgrad(L, fmt=1, s=None) == bsq.BSQ_ERR_INVALID_ARG
+    assert "bsq_linear_dgrad" in bsq.last_error()
+    assert L.bsq_dequant(0, FAKE, None, None, 1, 4, 32, FAKE, None) == bsq.BSQ_ERR_UNSUPPORTED
+    assert L.bsq_dequant(2, FAKE, FAKE, None, 1, 4, 48, FAKE, None) == bsq.BSQ_ERR_INVALID_ARG
+    assert L.bsq_grouped_dgrad(FAKE, 16, 128, 1, FAKE, FAKE, None, 0, 256, FAKE, FAKE, None) == \
+        bsq.BSQ_ERR_INVALID_ARG                                      # E = 0
+    assert L.bsq_grouped_dgrad(FAKE, 16, 128, 1, FAKE, FAKE, None, 2000, 256, FAKE, FAKE, None) == \
+        bsq.BSQ_ERR_UNSUPPORTED                                      # E above the limit
+    assert L.bsq_grouped_wgrad(FAKE, 16, 128, 1, FAKE, FAKE, None, 256, None, 4, FAKE, None) == \
+        bsq.BSQ_ERR_INVALID_ARG                                      # null offsets
+    code = ctypes.c_int32(0)
+    assert L.bsq_get_device_error(None, None) == bsq.BSQ_ERR_INVALID_ARG
+
+
+def test_empty_problems_return_ok_without_launch(L):
+    # K == 0 or M == 0 (dgrad) is a no-op that must not touch the device
+    assert _dgrad(L, M=0) == bsq.BSQ_OK
+    assert _dgrad(L, K=0) == bsq.BSQ_OK
+    assert L.bsq_dequant(1, FAKE, FAKE, None, 0, 4, 32, FAKE, None) == bsq.BSQ_OK

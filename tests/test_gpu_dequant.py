@@ -1,0 +1,41 @@
+"""bsq_dequant on the GPU against the oracle: bit-exact BF16 (every NaN one class)."""
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_gemm_fp8_gb300 import bsq, synth
+from tests._util import oracle_deq_bits, same_bits
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("kind", ["random", "edge", "nan"])
+@pytest.mark.parametrize("shape", [(1, 1, 32), (2, 129, 96), (3, 200, 352), (1, 64, 4096)])
+def test_dequant_bit_exact(fmt, kind, shape):
+    B, R, C = shape
+    p = synth.random_codes(fmt, B, R, C, seed=B * 1000 + R + C, scale_kind=kind)
+    ref = oracle_deq_bits(p).reshape(B, R, C)
+    out = bsq.dequant(p.to("cuda"))
+    torch.cuda.synchronize()
+    got = synth.bf16_numpy(out).reshape(B, R, C)
+    assert same_bits(got, ref), f"mismatches: {(got != ref).sum()}"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequant_quantized_values(fmt):
+    p = synth.make_packed(fmt, 2, 256, 512, 1.0, seed=3, device="cpu")
+    ref = oracle_deq_bits(p).reshape(2, 256, 512)
+    out = bsq.dequant(p.to("cuda"))
+    torch.cuda.synchronize()
+    assert same_bits(synth.bf16_numpy(out).reshape(2, 256, 512), ref)
+
+
+def test_dequant_leaves_no_device_error():
+    p = synth.random_codes(synth.FMT_MXFP4, 1, 16, 64, seed=1)
+    bsq.dequant(p.to("cuda"))
+    st, code = bsq.get_device_error()
+    assert st == bsq.BSQ_OK and code == 0
