@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled backward GEMMs on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl native|reference]
+
+One step = the backward of one layer on one batch of seeded synthetic input, entirely
+in libbsq's kernels: for the default workload (MXFP4 4096 x 4096 x 4096, W and X packed
+E2M1 with E8M0 per-32 scales) that is bsq_linear_dgrad + bsq_linear_wgrad.  L2 is
+flushed (a 256 MiB device memset, outside the timed events) before every timed step.
+Prints one JSON line.  ``value`` is TFLOP/s of the timed steps with inputs resident in
+HBM; ``e2e`` is the same metric through the same C ABI calls with the step's inputs
+copied from pinned host memory and both gradients copied back inside the timed region.
+The small-M (M = 16) dgrad of the same weight is reported as GB/s of algorithmic bytes.
+
+With --impl reference the CPU oracle is timed on a bounded sample of the same workload
+(the only other place the oracle runs besides the tests and the cpu_baseline leg).
+Multi-GPU (torchrun): every rank runs an independent replica (the path has no exchange
+step); value = all ranks' FLOPs / the slowest rank's time.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FMT_BYTES = {0: 2.0, 1: 1.0, 2: 0.5, 3: 0.5}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- work accounting
+def packed_bytes(p):
+    """Bytes of a packed operand including its scales (what the method must read)."""
+    n = p.batch * p.rows * p.cols
+    b = n * FMT_BYTES[p.fmt]
+    if p.fmt == 1:
+        b += 4 * p.batch * -(-p.rows // 128) * -(-p.cols // 128)
+    elif p.fmt == 2:
+        b += n / 32
+    elif p.fmt == 3:
+        b += n / 16 + 4 * p.batch
+    return b
+
+
+def plan(c):
+    """List of (name, flops, algorithmic_bytes) for the ops of one step of config c."""
+    M, N, K = c["M"], c["N"], c["K"]
+    ops = []
+    if not c["grouped"]:
+        ops.append(("dgrad", 2.0 * M * N * K, packed_bytes(c["W"]) + 2 * M * N + 2 * M * K))
+        ops.append(("wgrad", 2.0 * M * N * K, packed_bytes(c["X"]) + 2 * M * N + 2 * N * K))
+    else:
+        S = int(c["offsets"][-1])
+        ops.append(("grouped_dgrad", 2.0 * S * N * K, packed_bytes(c["W"]) + 2 * S * N + 2 * S * K))
+        if c["X"] is not None:
+            ops.append(("grouped_wgrad", 2.0 * S * N * K, packed_bytes(c["X"]) + 2 * S * N + 2 * c["E"] * N * K))
+    return ops
+
+
+# ---------------------------------------------------------------- peaks and clocks
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+
+        def find(keys):
+            for k in keys:
+                if k in d and isinstance(d[k], (int, float)):
+                    return float(d[k])
+            return None
+        hbm = find(["hbm_gbs", "hbm_GBps"])
+        bf16 = find(["bf16_tflops", "bf16_TFLOPs"])
+        if hbm and bf16:
+            return {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- native arm
+def run_ops(c, ops_out, bsq, stream=None):
+    """Launch one step; returns the number of library kernels launched."""
+    if not c["grouped"]:
+        bsq.linear_dgrad(c["G"], c["W"], out=ops_out["dgrad"], stream=stream)
+        bsq.linear_wgrad(c["G"], c["X"], out=ops_out["wgrad"], stream=stream)
+        return 2
+    bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=ops_out["grouped_dgrad"], stream=stream)
+    n = 1
+    if c["X"] is not None:
+        bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=ops_out["grouped_wgrad"], stream=stream)
+        n += 1
+    return n
+
+
+def alloc_outputs(c, dev):
+    M, N, K = c["M"], c["N"], c["K"]
+    if not c["grouped"]:
+        return {"dgrad": torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                "wgrad": torch.empty((N, K), dtype=torch.bfloat16, device=dev)}
+    o = {"grouped_dgrad": torch.empty((M, K), dtype=torch.bfloat16, device=dev)}
+    if c["X"] is not None:
+        o["grouped_wgrad"] = torch.empty((c["E"], N, K), dtype=torch.bfloat16, device=dev)
+    return o
+
+
+def time_ops(c, outs, bsq, steps, warmup, flush):
+    """Per-op CUDA-event times (ms) over `steps` L2-flushed steps, plus launches."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        run_ops(c, outs, bsq)
+    torch.cuda.synchronize()
+    names = list(outs.keys())
+    per_op = {n: [] for n in names}
+    step_ms = []
+    launches = 0
+    for _ in range(steps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        evs[0].record(stream)
+        for i, n in enumerate(names):
+            if not c["grouped"]:
+                (bsq.linear_dgrad(c["G"], c["W"], out=outs[n]) if n == "dgrad"
+                 else bsq.linear_wgrad(c["G"], c["X"], out=outs[n]))
+            elif n == "grouped_dgrad":
+                bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=outs[n])
+            else:
+                bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=outs[n])
+            launches += 1
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        for i, n in enumerate(names):
+            per_op[n].append(evs[i].elapsed_time(evs[i + 1]))
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
+    return per_op, step_ms, launches
+
+
+def time_small_m(c, bsq, steps, warmup, flush):
+    """M = 16 dgrad through the same weight: (median ms, algorithmic bytes)."""
+    G = c["G_small"]
+    out = torch.empty((G.shape[0], c["K"]), dtype=torch.bfloat16, device=G.device)
+    for _ in range(warmup):
+        bsq.linear_dgrad(G, c["W"], out=out)
+    torch.cuda.synchronize()
+    ts = []
+    stream = torch.cuda.current_stream()
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bsq.linear_dgrad(G, c["W"], out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    nbytes = packed_bytes(c["W"]) + 2 * G.numel() + 2 * G.shape[0] * c["K"]
+    return statistics.median(ts), nbytes
+
+
+def time_e2e(c, outs, bsq, steps, warmup):
+    """Same ops through the ABI with inputs copied from pinned host memory and results read back."""
+    dev = c["G"].device
+    host_in, dev_in = [], []
+
+    def pin(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host_in.append(h)
+        dev_in.append(t)
+
+    pin(c["G"])
+    for p in (c["W"], c["X"]):
+        if p is None:
+            continue
+        for t in (p.data, p.scale, p.tensor_scale):
+            if t is not None:
+                pin(t)
+    host_out = {n: torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for n, o in outs.items()}
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out.values())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        run_ops(c, outs, bsq)
+        for n, o in outs.items():
+            host_out[n].copy_(o, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------- the oracle as a baseline
+def oracle_sample(c, ncols, seed=0):
+    """Time the CPU oracle on ncols sampled output columns of every op of the step.
+
+    Returns (seconds, flops computed).  Dequantizes only the sampled columns of the
+    packed operand (as the oracle does for sampled parity checks) and runs the float64
+    products for them.
+    """
+    from oracle import dequant as D
+    from oracle import gemm as Gm
+    from block_scaled_gemm_fp8_gb300 import synth
+    names = {0: D.FMT_BF16, 1: D.FMT_FP8, 2: D.FMT_MXFP4, 3: D.FMT_NVFP4}
+    rng = np.random.default_rng(seed)
+    cols = np.sort(rng.choice(c["K"], size=min(ncols, c["K"]), replace=False))
+    g_bits = c["G_host"]
+    t0 = time.perf_counter()
+    g = Gm.as_f64(g_bits)
+    flops = 0.0
+    if not c["grouped"]:
+        for key, p in (("W", c["W"]), ("X", c["X"])):
+            d, s, ts = c[key + "_host"]
+            b = D.dequant_cols(names[p.fmt], d, s, ts, p.rows, p.cols, cols)
+            r = g @ b if key == "W" else g.T @ b
+            flops += 2.0 * r.shape[0] * g.shape[1 if key == "W" else 0] * len(cols)
+    else:
+        offs = c["offsets"]
+        d, s, ts = c["W_host"]
+        p = c["W"]
+        for e in range(c["E"]):
+            r0, r1 = Gm.expert_rows(offs, e)
+            if r1 > r0:
+                b = D.dequant_cols(names[p.fmt], d, s, ts, p.rows, p.cols, cols, e, p.batch)
+                _ = g[r0:r1] @ b
+                flops += 2.0 * (r1 - r0) * p.rows * len(cols)
+    return time.perf_counter() - t0, flops
+
+
+def host_copies(c):
+    from block_scaled_gemm_fp8_gb300 import synth
+    c["G_host"] = synth.bf16_numpy(c["G"])
+    for key in ("W", "X"):
+        if c.get(key) is not None:
+            c[key + "_host"] = c[key].numpy()
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from block_scaled_gemm_fp8_gb300 import synth
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        c = synth.make_config(args.config, device="cpu")
+        host_copies(c)
+        ops = plan(c)
+        ncols = 32
+        for _ in range(args.warmup):
+            oracle_sample(c, ncols, seed=1)
+        secs, flops = 0.0, 0.0
+        for k in range(args.steps):
+            s, f = oracle_sample(c, ncols, seed=2 + k)
+            secs += s
+            flops += f
+        value = flops / secs / 1e12
+        line = {"impl": "reference", "metric": "dgrad+wgrad TFLOP/s", "value": value, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": c["name"], "ops": [o[0] for o in ops]},
+                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                 "sample": f"{ncols} sampled output columns of every op per step"},
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from block_scaled_gemm_fp8_gb300 import bsq
+    bsq.lib()
+
+    c = synth.make_config(args.config, device=dev, seed=0)
+    if c["grouped"]:
+        c["offsets_dev"] = torch.from_numpy(c["offsets"]).to(dev)
+    outs = alloc_outputs(c, dev)
+    ops = plan(c)
+    flops_step = sum(o[1] for o in ops)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    per_op, step_ms, launches = time_ops(c, outs, bsq, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        total_ms = float(t.item())
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    st, code = bsq.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error {code} during the benchmark")
+
+    pk = peaks()
+    # dominant kernel: the op with the largest share of the step
+    avg = {n: statistics.mean(v) for n, v in per_op.items()}
+    dom = max(avg, key=avg.get)
+    dom_flops, dom_bytes = [(o[1], o[2]) for o in ops if o[0] == dom][0]
+    t_dom = avg[dom] * 1e-3
+    tensor_t = dom_flops / (pk["bf16_tflops"] * 1e12)
+    hbm_t = dom_bytes / (pk["hbm_gbs"] * 1e9)
+    if tensor_t >= hbm_t:
+        roof = {"bound": "tensor", "achieved": dom_flops / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = f"bsq_gemm_kernel ({dom})"
+    roof["peak_source"] = pk["source"]
+
+    line = {"metric": "dgrad+wgrad TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": c["name"], "M": c["M"], "N": c["N"], "K": c["K"], "E": c["E"],
+                       "ops": [o[0] for o in ops], "l2": "flushed by a 256 MiB memset before every timed step",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "per_op_ms": {n: statistics.median(v) for n, v in per_op.items()},
+            "per_op_tflops": {o[0]: o[1] / (statistics.median(per_op[o[0]]) * 1e-3) / 1e12 for o in ops},
+            "roofline": roof, "gpu_launches": launches, "clocks": clocks}
+
+    if args.config == 2:
+        ms, nbytes = time_small_m(c, bsq, args.steps, args.warmup, flush)
+        line["small_m_dgrad"] = {"M": int(c["G_small"].shape[0]), "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                                 "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                 "algorithmic_bytes": nbytes}
+    if not args.no_e2e:
+        ms, h2d, d2h = time_e2e(c, outs, bsq, max(3, args.steps // 2), 2)
+        line["e2e"] = {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_copies(c)
+        ncols = 256
+        secs, fl = oracle_sample(c, ncols)
+        line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle", "seconds": secs,
+                                "sample": f"{ncols} sampled output columns of every op (float64 oracle)"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
