@@ -96,29 +96,73 @@ __device__ __forceinline__ uint32_t apply_scale(uint32_t v2, const ScaleBf16& s,
   return s.fast ? bf16x2_mul(v2, s.c2) : bf16x2_mul(bf16x2_mul(v2, pow2k_x2), s.s2);
 }
 
-// 8 E2M1 codes (one 32-bit word, element j in bits 4j..4j+3) -> 4 BF16 pairs
-// out[i] = (element i, element i+4), scaled.
-__device__ __forceinline__ void decode_e2m1x8(uint32_t w, const ScaleBf16& s, uint32_t (&out)[4]) {
+// Scaled-down BF16 pairs of 8 E2M1 codes (one 32-bit word, element j in bits 4j..4j+3):
+// v[i] = (element i, element i+4), each = code value * 2^-126 with the code's sign.
+// A nibble s|eem isolated at bit b is spread by one integer multiply into two copies,
+// at b+6 (eem lands in BF16 exponent/mantissa bits 8:6) and b+12 (s lands in bit 15);
+// the mask keeps those fields and drops the other halves of the copies.  The two
+// nibbles of a pair sit 16 bits apart, so one multiply serves both.
+__device__ __forceinline__ void spread_e2m1x8(uint32_t w, uint32_t (&v)[4]) {
+  const uint32_t w8 = w >> 8;
+  v[0] = ((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;   // nibbles at bits 0, 16: shifts 6 and 12
+  v[1] = ((w & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;   // nibbles at bits 4, 20: shifts 2 and 8
+  v[2] = ((w8 & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+  v[3] = ((w8 & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+}
+
+__device__ __forceinline__ void scale_pairs4(uint32_t (&v)[4], const ScaleBf16& s, uint32_t pow2k_x2) {
+  if (s.fast) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t t = w >> (4 * i);
-    const uint32_t v = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
-    out[i] = apply_scale(v, s, kPow2_126x2);
+    for (int i = 0; i < 4; ++i) v[i] = bf16x2_mul(v[i], s.c2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = bf16x2_mul(bf16x2_mul(v[i], pow2k_x2), s.s2);
   }
+}
+
+// 8 E2M1 codes -> 4 BF16 pairs out[i] = (element i, element i+4), scaled.
+__device__ __forceinline__ void decode_e2m1x8(uint32_t w, const ScaleBf16& s, uint32_t (&out)[4]) {
+  spread_e2m1x8(w, out);
+  scale_pairs4(out, s, kPow2_126x2);
+}
+
+// Scaled-down BF16 pairs of 4 E4M3 codes (one word, element j in byte j):
+// a = (c0, c2), b = (c1, c3), each = code value * 2^-120 (NaN codes not handled here).
+__device__ __forceinline__ void spread_e4m3x4(uint32_t w, uint32_t& a, uint32_t& b) {
+  a = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
+  b = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
+}
+
+__device__ __forceinline__ bool e4m3_any_nan(uint32_t w) {
+  return (((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u;
+}
+
+// Overwrite the NaN codes of word w in its decoded pairs with BF16 NaN.
+__device__ __forceinline__ void e4m3_fix_nan(uint32_t w, uint32_t& p02, uint32_t& p13) {
+  if ((w & 0x0000007Fu) == 0x0000007Fu) p02 = (p02 & 0xFFFF0000u) | kBf16NaN;
+  if ((w & 0x00007F00u) == 0x00007F00u) p13 = (p13 & 0xFFFF0000u) | kBf16NaN;
+  if ((w & 0x007F0000u) == 0x007F0000u) p02 = (p02 & 0x0000FFFFu) | (kBf16NaN << 16);
+  if ((w & 0x7F000000u) == 0x7F000000u) p13 = (p13 & 0x0000FFFFu) | (kBf16NaN << 16);
 }
 
 // 4 E4M3 codes (one word, element j in byte j) -> 2 BF16 pairs (c0,c2),(c1,c3), scaled.
 __device__ __forceinline__ void decode_e4m3x4(uint32_t w, const ScaleBf16& s, uint32_t& p02, uint32_t& p13) {
-  const uint32_t a = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
-  const uint32_t b = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
-  p02 = apply_scale(a, s, kPow2_120x2);
-  p13 = apply_scale(b, s, kPow2_120x2);
+  spread_e4m3x4(w, p02, p13);
+  p02 = apply_scale(p02, s, kPow2_120x2);
+  p13 = apply_scale(p13, s, kPow2_120x2);
   // S.1111.111 is NaN in E4M3 (no infinities); the bit move above does not see it.
-  if (((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) {
-    if ((w & 0x0000007Fu) == 0x0000007Fu) p02 = (p02 & 0xFFFF0000u) | kBf16NaN;
-    if ((w & 0x00007F00u) == 0x00007F00u) p13 = (p13 & 0xFFFF0000u) | kBf16NaN;
-    if ((w & 0x007F0000u) == 0x007F0000u) p02 = (p02 & 0x0000FFFFu) | (kBf16NaN << 16);
-    if ((w & 0x7F000000u) == 0x7F000000u) p13 = (p13 & 0x0000FFFFu) | (kBf16NaN << 16);
+  if (e4m3_any_nan(w)) e4m3_fix_nan(w, p02, p13);
+}
+
+// 8 E4M3 codes (two words) -> one 8-element group as 4 BF16 pairs
+// (c0,c2),(c1,c3),(c4,c6),(c5,c7), scaled.
+__device__ __forceinline__ void decode_e4m3x8(uint32_t w0, uint32_t w1, const ScaleBf16& s, uint32_t (&out)[4]) {
+  spread_e4m3x4(w0, out[0], out[1]);
+  spread_e4m3x4(w1, out[2], out[3]);
+  scale_pairs4(out, s, kPow2_120x2);
+  if (e4m3_any_nan(w0 | w1)) {  // conservative: OR can only add candidates, the fix checks bytes
+    e4m3_fix_nan(w0, out[0], out[1]);
+    e4m3_fix_nan(w1, out[2], out[3]);
   }
 }
 

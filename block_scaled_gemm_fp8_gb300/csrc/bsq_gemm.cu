@@ -18,9 +18,10 @@
 //   warp 1      MMA issuer (one thread): tcgen05.mma 128 x N x 16, FP32 accumulators in TMEM
 //   warp 2      TMEM allocation / release
 //   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
-//   warps 8-15  dequantization: packed codes (smem) -> BF16, written in the 128-byte
-//               swizzled MN-major layout the tensor core reads; also zero the rows of a
-//               k-block that lie outside the current expert (wgrad)
+//   warps 8-23  dequantization, two teams of 8 warps taking alternate k-blocks:
+//               packed codes (smem) -> BF16, written in the 128-byte swizzled MN-major
+//               layout the tensor core reads; also zero the rows of a k-block that lie
+//               outside the current expert (wgrad)
 // Stage hand-off: full[s] (TMA bytes landed) -> ready[s] (dequant done) -> empty[s]
 // (MMA done, tcgen05.commit).  Two TMEM accumulators (2 x 256 columns) let the
 // epilogue of one tile overlap the main loop of the next.  Tiles are walked in a
@@ -39,7 +40,8 @@ namespace bsq {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kDeqTeams = 2;                    // dequant teams alternate k-blocks
+constexpr int kThreads = 256 + kDeqTeams * 256;  // 8 control/epilogue warps + 8 warps per team
 constexpr int kBoxBytes = 64 * 64 * 2;          // one 64x64 BF16 box = one swizzle column of 64 rows
 constexpr int kABytes = kTileM * kTileK * 2;     // 16 KB: dequantized operand, 2 swizzle columns
 constexpr int kBBytes = kTileN * kTileK * 2;     // 32 KB: grad_out side, 4 boxes
@@ -47,10 +49,13 @@ constexpr int kTmemCols = 512;                   // 2 accumulators x 256 FP32 co
 
 template <int FMT>
 struct Fmt {
+  static constexpr bool kFp4 = FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4;
   static constexpr int kPBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileK * kTileM : (FMT == BSQ_BF16 ? 0 : kTileK * kTileM / 2);
   static constexpr int kPRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileM : kTileM / 2;
+  // FP4 scale tile staged by TMA: 64 rows x 16 bytes (a 16-byte aligned window of the row's scales)
+  static constexpr int kSBytes = kFp4 ? kTileK * 16 : 0;
   static constexpr int kStages = FMT == BSQ_FP8_E4M3_B128 ? 3 : 4;
-  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes + kSBytes;
 };
 
 struct Params {
@@ -68,6 +73,7 @@ struct Params {
   int32_t num_m;              // ceil(Kc / 128)
   int32_t scale_ld;           // scale row pitch (elements)
   int32_t scale_rblocks;      // FP8: ceil(p_rows / 128)
+  int32_t scale_tma;          // FP4: scale tiles come through TMA (row pitch a multiple of 16 bytes)
   uint64_t timeout_ns;
 };
 
@@ -95,8 +101,8 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
@@ -141,7 +147,7 @@ __device__ __forceinline__ int lane_to_col(int i) {
 template <int FMT, int OP>
 __global__ void __launch_bounds__(kThreads, 1)
     bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_g,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tm_s, const Params p) {
   using F = Fmt<FMT>;
   constexpr int kStages = F::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -156,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto stage_a = [&](int s) { return smem + s * F::kStageBytes; };
   auto stage_b = [&](int s) { return smem + s * F::kStageBytes + kABytes; };
   auto stage_p = [&](int s) { return smem + s * F::kStageBytes + kABytes + kBBytes; };
+  auto stage_s = [&](int s) { return smem + s * F::kStageBytes + kABytes + kBBytes + F::kPBytes; };
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
@@ -175,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tm_p);
     tma_prefetch_map(&tm_g);
+    if (F::kFp4 && p.scale_tma) tma_prefetch_map(&tm_s);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
@@ -244,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, p.err, limit)) break;
           const uint32_t full = smem_u32(&sh.full[stage]);
-          const uint32_t bytes = (FMT == BSQ_BF16 ? 2 * kBoxBytes : F::kPBytes) + nbox * kBoxBytes;
+          const uint32_t bytes = (FMT == BSQ_BF16 ? 2 * kBoxBytes : F::kPBytes) + nbox * kBoxBytes +
+                                 ((F::kFp4 && p.scale_tma) ? F::kSBytes : 0);
           mbar_arrive_expect_tx(full, bytes);
           pend_mask |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -256,6 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             const int x = FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2;
             tma_load_3d(smem_u32(stage_p(stage)), &tm_p, full, x, prow, pbatch);
+            if (F::kFp4 && p.scale_tma) {
+              // 16-byte aligned window holding this tile's scales (4 or 8 bytes per row)
+              const int xs = (FMT == BSQ_MXFP4 ? (m0 >> 5) : (m0 >> 4)) & ~15;
+              tma_load_3d(smem_u32(stage_s(stage)), &tm_s, full, xs, prow, pbatch);
+            }
           }
           for (int j = 0; j < nbox; ++j) {
             if (OP == kDgrad)
@@ -371,78 +385,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 8) {
     // ===== dequantization =====
-    const int dw = warp - 8;  // 0..7
-    int stage = 0;
-    uint32_t phase = 0;
+    // Thread -> (row r of the k-block, group g of 32 columns).  A quarter-warp covers 4
+    // consecutive rows x 2 groups, so its 16-byte stores into the swizzled tile hit 8
+    // distinct bank groups; each thread needs one MX scale (two NVFP4, one FP8 block).
+    const int team = (warp - 8) >> 3;
+    const int dw = (warp - 8) & 7;                             // 0..7 within the team
+    const int qtr = lane >> 3;
+    const int r = dw * 8 + (qtr & 1) * 4 + (lane & 3);          // 0..63
+    const int g = (qtr >> 1) * 2 + ((lane >> 2) & 1);           // 0..3
+    uint32_t kcount = 0;                                       // k-blocks seen so far (all teams)
     int e_cur = 0;
     for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
       const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
       const int m0 = ti.mt * kTileM;
+      const int col0 = m0 + 32 * g;
+      const bool col_ok = col0 < p.Kc;
       const int pbatch = OP == kDgrad ? ti.e : 0;
       float tscale = 0.f;
       if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + pbatch);
       bool ok = true;
-      for (int kb = 0; kb < ti.kblocks; ++kb) {
-        // rows of this k-block that belong to the contraction
+      for (int kb = 0; kb < ti.kblocks; ++kb, ++kcount) {
+        if (static_cast<int>(kcount % kDeqTeams) != team) continue;
+        const int stage = static_cast<int>(kcount % kStages);
+        const uint32_t phase = (kcount / kStages) & 1u;
         const int prow0 = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
         const int kvalid = OP == kDgrad ? min(kTileK, p.N - kb * kTileK) : min(kTileK, ti.r1 - prow0);
-        // Scale bytes for this thread's 4 chunks, fetched before the wait.
-        uint32_t sraw[4];
-        float sf[4];
-        if (FMT != BSQ_BF16) {
-#pragma unroll
-          for (int ps = 0; ps < 4; ++ps) {
-            const int r = ps * 16 + dw * 2 + (lane >> 4);
-            const int col = m0 + 8 * (lane & 15);
-            sraw[ps] = 0;
-            sf[ps] = 0.f;
-            if (r < kvalid && col < p.Kc) {
-              const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + r;
-              if (FMT == BSQ_MXFP4)
-                sraw[ps] = __ldg(p.scale + grow * p.scale_ld + (col >> 5));
-              else if (FMT == BSQ_NVFP4)
-                sraw[ps] = __ldg(p.scale + grow * p.scale_ld + (col >> 4));
-              else
-                sf[ps] = __ldg(reinterpret_cast<const float*>(p.scale) +
-                               (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + r) >> 7)) * p.scale_ld +
-                               (col >> 7));
-            }
-          }
+        const bool valid = r < kvalid && col_ok;
+        const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + r;
+        // Scales that do not come through TMA are fetched before the wait.
+        uint32_t sraw = 0;
+        float sf = 0.f;
+        if (valid) {
+          if (FMT == BSQ_FP8_E4M3_B128)
+            sf = __ldg(reinterpret_cast<const float*>(p.scale) +
+                       (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + r) >> 7)) * p.scale_ld + (col0 >> 7));
+          else if (FMT == BSQ_MXFP4 && !p.scale_tma)
+            sraw = __ldg(p.scale + grow * p.scale_ld + (col0 >> 5));
+          else if (FMT == BSQ_NVFP4 && !p.scale_tma)
+            sraw = static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4))) |
+                   (static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
         }
         ok = wait_phase(smem_u32(&sh.full[stage]), phase, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         uint8_t* a_tile = stage_a(stage);
         if (FMT != BSQ_BF16) {
-          const uint8_t* p_tile = stage_p(stage);
-#pragma unroll
-          for (int ps = 0; ps < 4; ++ps) {
-            const int r = ps * 16 + dw * 2 + (lane >> 4);
-            const int c = lane & 15;
-            const bool valid = r < kvalid && (m0 + 8 * c) < p.Kc;
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (valid) {
-              if (FMT == BSQ_FP8_E4M3_B128) {
-                const uint2 w = *reinterpret_cast<const uint2*>(p_tile + r * F::kPRowBytes + c * 8);
-                const ScaleBf16 s = make_scale_fp8(sf[ps]);
-                decode_e4m3x4(w.x, s, o.x, o.y);
-                decode_e4m3x4(w.y, s, o.z, o.w);
-              } else {
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(p_tile + r * F::kPRowBytes + c * 4);
-                const ScaleBf16 s = FMT == BSQ_MXFP4 ? make_scale_e8m0(sraw[ps]) : make_scale_nvfp4(sraw[ps], tscale);
-                uint32_t pr[4];
-                decode_e2m1x8(w, s, pr);
-                o = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+          uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
+          if (valid) {
+            const uint8_t* prow = stage_p(stage) + r * F::kPRowBytes;
+            if (F::kFp4) {
+              if (p.scale_tma) {
+                const uint8_t* srow = stage_s(stage) + r * 16;
+                if (FMT == BSQ_MXFP4)
+                  sraw = srow[((m0 >> 5) & 15) + g];
+                else
+                  sraw = *reinterpret_cast<const uint16_t*>(srow + ((m0 >> 4) & 15) + 2 * g);
               }
+              const uint4 w = *reinterpret_cast<const uint4*>(prow + 16 * g);
+              ScaleBf16 s0, s1;
+              if (FMT == BSQ_MXFP4) {
+                s0 = make_scale_e8m0(sraw);
+                s1 = s0;
+              } else {
+                s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
+                s1 = make_scale_nvfp4(sraw >> 8, tscale);
+              }
+              decode_e2m1x8(w.x, s0, v[0]);
+              decode_e2m1x8(w.y, s0, v[1]);
+              decode_e2m1x8(w.z, s1, v[2]);
+              decode_e2m1x8(w.w, s1, v[3]);
+            } else {
+              // rows 128 bytes apart share banks: odd rows read their second half first
+              const int h = r & 1;
+              uint4 wa = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * h);
+              uint4 wb = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * (h ^ 1));
+              if (h) {
+                const uint4 t = wa;
+                wa = wb;
+                wb = t;
+              }
+              const ScaleBf16 s0 = make_scale_fp8(sf);
+              decode_e4m3x8(wa.x, wa.y, s0, v[0]);
+              decode_e4m3x8(wa.z, wa.w, s0, v[1]);
+              decode_e4m3x8(wb.x, wb.y, s0, v[2]);
+              decode_e4m3x8(wb.z, wb.w, s0, v[3]);
             }
-            const int atom = c >> 3, ch = c & 7;
-            *reinterpret_cast<uint4*>(a_tile + atom * kBoxBytes + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[j][i] = 0u;
+          }
+          // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
+          // 16-byte slot (4(g&1) + j) XOR (r & 7)
+          uint8_t* rowp = a_tile + (g >> 1) * kBoxBytes + r * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int slot = ((g & 1) * 4 + j) ^ (r & 7);
+            *reinterpret_cast<uint4*>(rowp + (slot << 4)) = make_uint4(v[j][0], v[j][1], v[j][2], v[j][3]);
           }
         } else if (kvalid < kTileK) {
           // BF16 operand from TMA: zero the rows outside the contraction
-          for (int idx = dw * 32 + lane; idx < (kTileK - kvalid) * 16; idx += 256) {
-            const int r = kvalid + idx / 16, c = idx % 16;
-            *reinterpret_cast<uint4*>(a_tile + (c >> 3) * kBoxBytes + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          const int dt = dw * 32 + lane;
+          for (int idx = dt; idx < (kTileK - kvalid) * 16; idx += 256) {
+            const int rr = kvalid + idx / 16, c = idx % 16;
+            *reinterpret_cast<uint4*>(a_tile + (c >> 3) * kBoxBytes + rr * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         if (OP == kWgrad && kvalid < kTileK) {
@@ -450,17 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // reach the products: zero them in every loaded box.
           uint8_t* b_tile = stage_b(stage);
           const int nbox = (ti.n_valid + 63) >> 6;
-          for (int idx = dw * 32 + lane; idx < (kTileK - kvalid) * 8 * nbox; idx += 256) {
+          const int dt = dw * 32 + lane;
+          for (int idx = dt; idx < (kTileK - kvalid) * 8 * nbox; idx += 256) {
             const int box = idx / ((kTileK - kvalid) * 8);
             const int rem = idx % ((kTileK - kvalid) * 8);
-            const int r = kvalid + rem / 8, c = rem % 8;
-            *reinterpret_cast<uint4*>(b_tile + box * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            const int rr = kvalid + rem / 8, c = rem % 8;
+            *reinterpret_cast<uint4*>(b_tile + box * kBoxBytes + rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.ready[stage]));
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
@@ -540,7 +587,25 @@ int launch_typed(const GemmArgs& a, const char** msg) {
       return -1;
     }
   }
+  // FP4 scale tiles through TMA when the scale row pitch is a multiple of 16 bytes.
+  CUtensorMap tm_s = tm_p;
+  int scale_tma = 0;
+  if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) {
+    const uint64_t srow = FMT == BSQ_MXFP4 ? a.kc / 32 : a.kc / 16;
+    if (srow % 16 == 0 && (reinterpret_cast<uintptr_t>(a.p_scale) & 15u) == 0) {
+      const uint64_t dims[3] = {srow, static_cast<uint64_t>(a.p_rows), static_cast<uint64_t>(a.p_batch)};
+      const uint64_t strides[2] = {srow, srow * static_cast<uint64_t>(a.p_rows)};
+      const uint32_t box[3] = {16, static_cast<uint32_t>(kTileK), 1};
+      if (!encode_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.p_scale, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        *msg = "tensor map encoding failed for the scales";
+        return -1;
+      }
+      scale_tma = 1;
+    }
+  }
   Params p;
+  p.scale_tma = scale_tma;
   p.scale = static_cast<const uint8_t*>(a.p_scale);
   p.tensor_scale = a.p_tensor_scale;
   p.offsets = a.offsets;
@@ -568,7 +633,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   auto kern = bsq_gemm_kernel<FMT, OP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) {
-    kern<<<dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, a.stream>>>(tm_p, tm_g, p);
+    kern<<<dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, a.stream>>>(tm_p, tm_g, tm_s, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

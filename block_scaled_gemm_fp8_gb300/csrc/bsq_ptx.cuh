@@ -43,6 +43,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
   return ok;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds waiting for the phase.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok;
+}
+
 // Proxy fence: generic-proxy shared-memory writes become visible to the async proxy
 // (tensor core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
