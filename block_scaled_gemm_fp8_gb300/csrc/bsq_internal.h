@@ -55,6 +55,23 @@ struct DequantArgs {
 
 int launch_dequant(const DequantArgs& a, const char** msg);
 
+struct SmallMArgs {
+  int fmt;
+  const void* g;          // bf16 [M][N]
+  const void* w_data;     // packed [N][K]
+  const void* w_scale;
+  const float* w_tensor_scale;
+  int64_t M, N, K;        // M <= 16
+  void* out;              // bf16 [M][K]
+  void* ws;               // FP32 workspace of smallm_workspace_bytes(K) bytes, zero between calls
+  int num_sms;
+  cudaStream_t stream;
+};
+
+constexpr int kSmallM = 16;  // dgrad with at most this many rows takes the split-K kernel
+size_t smallm_workspace_bytes(int64_t K);
+int launch_smallm(const SmallMArgs& a, const char** msg);
+
 // Wait limit of every pipeline wait inside the kernels (nanoseconds of %globaltimer).
 uint64_t wait_limit_ns();
 
