@@ -30,6 +30,8 @@ SIGNATURES = {
                           _c_void_p, _c_void_p],
     "bsq_grouped_wgrad": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64,
                           _c_void_p, _c_void_p],
+    "bsq_linear_dgrad_smallm_noalloc": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64,
+                                        _c_void_p, _c_void_p],
     "bsq_status_string": [_i32],
     "bsq_last_error": [],
     "bsq_get_device_error": [ctypes.POINTER(_i32), _c_void_p],
@@ -119,6 +121,17 @@ def linear_dgrad(grad_out, w, out=None, stream=None):
         out = torch.empty((M, w.cols), dtype=torch.bfloat16, device=grad_out.device)
     _check(lib().bsq_linear_dgrad(_ptr(grad_out), M, N, w.fmt, _ptr(w.data), _ptr(w.scale), _ptr(w.tensor_scale),
                                   w.cols, _ptr(out), _stream(stream)))
+    return out
+
+
+def linear_dgrad_smallm_noalloc(grad_out, w, out=None, stream=None):
+    """grad_x[M,K] = grad_out[M,N] @ deq(W)[N,K] for M <= 16 without any device allocation
+    (split-K scratch in a static device array of the library; K <= 16384)."""
+    M, N = grad_out.shape
+    if out is None:
+        out = torch.empty((M, w.cols), dtype=torch.bfloat16, device=grad_out.device)
+    _check(lib().bsq_linear_dgrad_smallm_noalloc(_ptr(grad_out), M, N, w.fmt, _ptr(w.data), _ptr(w.scale),
+                                                 _ptr(w.tensor_scale), w.cols, _ptr(out), _stream(stream)))
     return out
 
 

@@ -155,6 +155,15 @@ bsq_status zero_output(void* out, int64_t bytes, cudaStream_t s, const char* wha
 }  // namespace
 
 namespace bsq {
+int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
+                            const void* w_scale, const float* w_tensor_scale, int64_t K, const void* grad_x) {
+  bsq_status st = check_gemm_common("bsq_linear_dgrad", grad_out, M, N, w_fmt, K, grad_x);
+  if (st != BSQ_OK) return st;
+  return check_packed("bsq_linear_dgrad", w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, true);
+}
+int set_error(int status, const char* message) {
+  return fail(static_cast<bsq_status>(status), "%s", message);
+}
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* s = std::getenv("BSQ_WAIT_LIMIT_MS");

@@ -72,6 +72,12 @@ constexpr int kSmallM = 16;  // dgrad with at most this many rows takes the spli
 size_t smallm_workspace_bytes(int64_t K);
 int launch_smallm(const SmallMArgs& a, const char** msg);
 
+// Host-side argument checks of bsq_linear_dgrad (bsq_api.cu); BSQ_OK when well formed.
+int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
+                            const void* w_scale, const float* w_tensor_scale, int64_t K, const void* grad_x);
+// Record a message for bsq_last_error() and return `status`.
+int set_error(int status, const char* message);
+
 // Wait limit of every pipeline wait inside the kernels (nanoseconds of %globaltimer).
 uint64_t wait_limit_ns();
 

@@ -14,6 +14,9 @@
 //   * m16n8k16 BF16 mma.sync with FP32 accumulators (tokens are the M=16 side);
 //   * the CTAs of a slab reduce through an FP32 workspace with atomics; the last CTA to
 //     finish a slab converts it to BF16, writes grad_X and zeroes the workspace again.
+#include <cstdio>
+#include <mutex>
+
 #include <cuda_bf16.h>
 
 #include "bsq_decode.cuh"
@@ -350,3 +353,80 @@ int launch_smallm(const SmallMArgs& a, const char** msg) {
 }
 
 }  // namespace bsq
+
+// ---------------------------------------------------------------- allocation-free entry point
+// Some callers cannot call cudaMalloc at all: code running inside a CUDA graph that is being
+// captured, allocators that own every byte of device memory, or hosts that forbid device
+// allocation after start-up.  bsq_linear_dgrad_smallm_noalloc serves them with the small-M
+// kernel above, its split-K scratch living in this file-scope device array instead of the
+// lazily allocated workspace.  The array exists on every device that loads the library,
+// for the life of the process.
+namespace {
+
+constexpr int64_t kStaticMaxK = 16384;  // largest K the static scratch serves
+constexpr size_t kStaticScratchBytes = 16 * kStaticMaxK * 4 + 4096;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevicesStatic = 64;
+void* g_static_ptr[kMaxDevicesStatic] = {};
+int g_static_sms[kMaxDevicesStatic] = {};
+std::mutex g_static_mu;
+
+}  // namespace
+
+extern "C" bsq_status bsq_linear_dgrad_smallm_noalloc(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt,
+                                                      const void* w_data, const void* w_scale,
+                                                      const float* w_tensor_scale, int64_t K, void* grad_x,
+                                                      void* stream) {
+  const int st = bsq::check_linear_dgrad_args(grad_out, M, N, w_fmt, w_data, w_scale, w_tensor_scale, K, grad_x);
+  if (st != BSQ_OK) return static_cast<bsq_status>(st);
+  if (M > bsq::kSmallM)
+    return static_cast<bsq_status>(
+        bsq::set_error(BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: M must be <= 16"));
+  if (w_fmt == BSQ_BF16)
+    return static_cast<bsq_status>(
+        bsq::set_error(BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: W must be FP8, MXFP4 or NVFP4"));
+  if (K > kStaticMaxK || bsq::smallm_workspace_bytes(K) > kStaticScratchBytes)
+    return static_cast<bsq_status>(bsq::set_error(
+        BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: K exceeds the static scratch maximum of 16384"));
+  if (M == 0 || K == 0) return BSQ_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    const cudaError_t e = cudaMemsetAsync(grad_x, 0, static_cast<size_t>(M * K * 2), s);
+    return e == cudaSuccess ? BSQ_OK
+                            : static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, cudaGetErrorString(e)));
+  }
+  // Per-device set-up on the first call (device current): the array's device address.
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevicesStatic)
+    return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, "bsq_linear_dgrad_smallm_noalloc: no device"));
+  void* scratch = nullptr;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+      if (e != cudaSuccess)
+        return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, cudaGetErrorString(e)));
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess)
+        return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, cudaGetErrorString(e)));
+      g_static_ptr[dev] = ptr;
+      g_static_sms[dev] = n;
+    }
+    scratch = g_static_ptr[dev];
+    sms = g_static_sms[dev];
+  }
+  // The kernel needs the scratch at zero on entry (and leaves it so); clear the part this
+  // call uses so that an earlier interrupted call cannot leak into this one.
+  e = cudaMemsetAsync(scratch, 0, bsq::smallm_workspace_bytes(K), s);
+  if (e != cudaSuccess) return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, cudaGetErrorString(e)));
+  bsq::SmallMArgs a{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, M, N, K, grad_x, scratch, sms, s};
+  const char* msg = "";
+  if (bsq::launch_smallm(a, &msg) != 0) return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, msg));
+  return BSQ_OK;
+}
+

@@ -42,7 +42,11 @@
  *     (an alignment above, too many experts); BSQ_ERR_CUDA a failed launch.
  *     Device-side conditions (decreasing offsets, a pipeline wait that ran out of
  *     time) are recorded in a per-device error word read by bsq_get_device_error.
- *   - Allocation: the library allocates no device memory per call.
+ *   - Allocation: the caller owns every tensor.  The library's own device memory is one
+ *     error word per device and, for bsq_linear_dgrad with M <= 16, one FP32 split-K
+ *     workspace per device (16*K*4 bytes plus counters, at least 1 MiB) that the first such
+ *     call allocates and a later call with a larger K re-allocates; make the first small-M
+ *     call before any stream capture.  bsq_linear_dgrad_smallm_noalloc allocates nothing.
  */
 #ifndef BSQ_H
 #define BSQ_H
@@ -86,6 +90,8 @@ bsq_status bsq_dequant(int32_t fmt, const void* data, const void* scale, const f
  * bsq_linear_dgrad -- grad_x[M][K] = grad_out[M][N] @ deq(W)[N][K]
  * (MSLK PR #393, Implementation Method; transformers PR #50031 FP8LinearFunction.backward).
  * grad_out: bf16[M][N]; W: packed [1][N][K] in w_fmt; grad_x: bf16[M][K] (fully written).
+ * M <= 16 with a packed W takes a split-K kernel whose partial sums meet in the per-device
+ * workspace: such calls on one device must not overlap in time (different streams).
  */
 bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N,
                             int32_t w_fmt, const void* w_data, const void* w_scale,
@@ -124,6 +130,28 @@ bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N,
                              int32_t x_fmt, const void* x_data, const void* x_scale,
                              const float* x_tensor_scale, int64_t K, const int32_t* offsets,
                              int64_t E, void* grad_w, void* stream);
+
+/*
+ * bsq_linear_dgrad_smallm_noalloc -- the same product as bsq_linear_dgrad, for callers that
+ * cannot allocate device memory (code running under stream capture, hosts whose allocator
+ * owns all device memory, or processes that forbid allocation after start-up).  The pages
+ * have no counterpart: it is an allocation-free variant of this library's split-K small-M
+ * dgrad kernel.  Its FP32 split-K scratch is a file-scope device array of the library, not
+ * the lazily allocated workspace bsq_linear_dgrad uses; every device that loads the library
+ * holds that array (about 1 MiB) until the process exits.
+ * Limits: 1 <= M <= 16, w_fmt FP8 / MXFP4 / NVFP4, K <= 16384; anything else returns
+ * BSQ_ERR_UNSUPPORTED (or the usual argument errors) without launching.
+ * Allocation: calls no cudaMalloc / cudaFree or any allocating routine.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.
+ * Sharing: every call uses the same array and clears the part it needs on `stream` before
+ * its kernel; calls whose work overlaps on the GPU (different streams) race on the array
+ * and must be ordered by the caller.
+ */
+bsq_status bsq_linear_dgrad_smallm_noalloc(const void* grad_out, int64_t M, int64_t N,
+                                           int32_t w_fmt, const void* w_data, const void* w_scale,
+                                           const float* w_tensor_scale, int64_t K, void* grad_x,
+                                           void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* bsq_status_string(int32_t status);
