@@ -13,8 +13,9 @@
 // "MN-major" A operand: no transpose kernel is needed on either side, and the
 // dequantization work per tensor-core FLOP is that of a 128-row operand.
 //
-// One persistent CTA per SM, 16 warps:
-//   warp 0      TMA producer: packed tile (or BF16 tile) + grad_out boxes per stage
+// One persistent CTA per SM, 24 warps:
+//   warp 0      TMA producer of the packed ring: packed tile (+ FP4 scale tile) per k-block
+//   warp 3      TMA producer of the grad_out ring: up to four 64x64 BF16 boxes per k-block
 //   warp 1      MMA issuer (one thread): tcgen05.mma 128 x N x 16, FP32 accumulators in TMEM
 //   warp 2      TMEM allocation / release
 //   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
@@ -22,12 +23,14 @@
 //               packed codes (smem) -> BF16, written in the 128-byte swizzled MN-major
 //               layout the tensor core reads; also zero the rows of a k-block that lie
 //               outside the current expert (wgrad)
-// Stage hand-off: full[s] (TMA bytes landed) -> ready[s] (dequant done) -> empty[s]
-// (MMA done, tcgen05.commit).  Two TMEM accumulators (2 x 256 columns) let the
-// epilogue of one tile overlap the main loop of the next.  Tiles are walked in a
-// static persistent order; the expert of a tile comes from a per-CTA prefix sum of
-// tile counts over the offsets.  Every wait is bounded by %globaltimer and records a
-// timeout in the device error word instead of hanging.
+// Three rings decouple the chains: the packed ring (deep, small stages) feeds the
+// dequant teams; the BF16 operand ring feeds the MMA from the dequant teams; the
+// grad_out ring feeds the MMA straight from TMA.  Each buffer is held only for its own
+// chain, so TMA latency, decode time and MMA time overlap.  Two TMEM accumulators
+// (2 x 256 columns) let the epilogue of one tile overlap the main loop of the next.
+// Tiles are walked in a static persistent order; the expert of a tile comes from a
+// per-CTA prefix sum of tile counts over the offsets.  Every wait is bounded by
+// %globaltimer and records a timeout in the device error word instead of hanging.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -46,16 +49,23 @@ constexpr int kBoxBytes = 64 * 64 * 2;          // one 64x64 BF16 box = one swiz
 constexpr int kABytes = kTileM * kTileK * 2;     // 16 KB: dequantized operand, 2 swizzle columns
 constexpr int kBBytes = kTileN * kTileK * 2;     // 32 KB: grad_out side, 4 boxes
 constexpr int kTmemCols = 512;                   // 2 accumulators x 256 FP32 columns
+constexpr int kAStages = 3;
+constexpr int kBStages = 4;
+constexpr int kMaxStages = 8;
 
 template <int FMT>
 struct Fmt {
   static constexpr bool kFp4 = FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4;
-  static constexpr int kPBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileK * kTileM : (FMT == BSQ_BF16 ? 0 : kTileK * kTileM / 2);
+  // packed tile of one k-block (BF16: the operand tile itself, already swizzled by TMA)
+  static constexpr int kPBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileK * kTileM
+                                 : FMT == BSQ_BF16       ? kABytes
+                                                         : kTileK * kTileM / 2;
   static constexpr int kPRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileM : kTileM / 2;
   // FP4 scale tile staged by TMA: 64 rows x 16 bytes (a 16-byte aligned window of the row's scales)
   static constexpr int kSBytes = kFp4 ? kTileK * 16 : 0;
-  static constexpr int kStages = FMT == BSQ_FP8_E4M3_B128 ? 3 : 4;
-  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes + kSBytes;
+  static constexpr int kPStageBytes = (kPBytes + kSBytes + 1023) / 1024 * 1024;
+  static constexpr int kPStages = FMT == BSQ_BF16 ? 2 : (FMT == BSQ_FP8_E4M3_B128 ? 5 : 6);
+  static constexpr int kRingBytes = kBStages * kBBytes + kAStages * kABytes + kPStages * kPStageBytes;
 };
 
 struct Params {
@@ -78,9 +88,12 @@ struct Params {
 };
 
 struct SharedTail {
-  uint64_t full[4];
-  uint64_t ready[4];
-  uint64_t empty[4];
+  uint64_t p_full[kMaxStages];
+  uint64_t p_empty[kMaxStages];
+  uint64_t a_full[kMaxStages];
+  uint64_t a_empty[kMaxStages];
+  uint64_t b_full[kMaxStages];
+  uint64_t b_empty[kMaxStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -95,9 +108,8 @@ struct SharedTail {
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 
 // Bounded wait on an mbarrier phase; false when the CTA aborted or the limit ran out.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                        int32_t* err, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             int32_t* err, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
@@ -110,6 +122,21 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                           int32_t* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort_flag, err, limit_ns);
+}
+
+// Ring position of the kc-th k-block: slot and the parity of the phase it fills.
+struct Slot {
+  int idx;
+  uint32_t par;
+};
+template <int N>
+__device__ __forceinline__ Slot ring_slot(uint32_t kc) {
+  return Slot{static_cast<int>(kc % N), (kc / N) & 1u};
 }
 
 struct TileInfo {
@@ -144,32 +171,48 @@ __device__ __forceinline__ int lane_to_col(int i) {
   return i;
 }
 
+// Let the TMA copies this thread issued into the given slots land (orderly abort).
+template <int N>
+__device__ __forceinline__ void drain_pending(uint64_t* full, uint32_t mask, uint32_t par, uint64_t limit) {
+  for (int s = 0; s < N; ++s)
+    if (mask & (1u << s)) {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_u32(&full[s]), (par >> s) & 1u) && global_timer_ns() - t0 < limit) {
+      }
+    }
+}
+
 template <int FMT, int OP>
 __global__ void __launch_bounds__(kThreads, 1)
     bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_g,
                     const __grid_constant__ CUtensorMap tm_s, const Params p) {
   using F = Fmt<FMT>;
-  constexpr int kStages = F::kStages;
+  constexpr int kPStages = F::kPStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SharedTail& sh = *reinterpret_cast<SharedTail*>(smem + kStages * F::kStageBytes);
+  uint8_t* ring_b = smem;
+  uint8_t* ring_a = ring_b + kBStages * kBBytes;
+  uint8_t* ring_p = ring_a + kAStages * kABytes;
+  SharedTail& sh = *reinterpret_cast<SharedTail*>(smem + F::kRingBytes);
   volatile uint32_t* abort_flag = &sh.abort_flag;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  auto stage_a = [&](int s) { return smem + s * F::kStageBytes; };
-  auto stage_b = [&](int s) { return smem + s * F::kStageBytes + kABytes; };
-  auto stage_p = [&](int s) { return smem + s * F::kStageBytes + kABytes + kBBytes; };
-  auto stage_s = [&](int s) { return smem + s * F::kStageBytes + kABytes + kBBytes + F::kPBytes; };
-
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sh.full[s]), 1);
-      mbar_init(smem_u32(&sh.ready[s]), 8);
-      mbar_init(smem_u32(&sh.empty[s]), 1);
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(smem_u32(&sh.p_full[s]), 1);
+      mbar_init(smem_u32(&sh.p_empty[s]), 8);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(smem_u32(&sh.a_full[s]), 8);
+      mbar_init(smem_u32(&sh.a_empty[s]), 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(smem_u32(&sh.b_full[s]), 1);
+      mbar_init(smem_u32(&sh.b_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sh.tmem_full[b]), 1);
@@ -239,65 +282,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- roles
   if (warp == 0) {
-    // ===== TMA producer =====
+    // ===== TMA producer: packed ring =====
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      uint32_t kc = 0;
       int e_cur = 0;
-      uint32_t pend_mask = 0, pend_par = 0;  // stages with loads in flight (for an orderly abort)
+      uint32_t pend_mask = 0, pend_par = 0;
       for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
         const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
         const int m0 = ti.mt * kTileM;
-        const int nbox = (ti.n_valid + 63) >> 6;
-        for (int kb = 0; kb < ti.kblocks; ++kb) {
-          if (!wait_phase(smem_u32(&sh.empty[stage]), phase ^ 1u, abort_flag, p.err, limit)) break;
-          const uint32_t full = smem_u32(&sh.full[stage]);
-          const uint32_t bytes = (FMT == BSQ_BF16 ? 2 * kBoxBytes : F::kPBytes) + nbox * kBoxBytes +
-                                 ((F::kFp4 && p.scale_tma) ? F::kSBytes : 0);
-          mbar_arrive_expect_tx(full, bytes);
-          pend_mask |= 1u << stage;
-          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+        const int pbatch = OP == kDgrad ? ti.e : 0;
+        bool ok = true;
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
+          const Slot sl = ring_slot<kPStages>(kc);
+          if (!wait_phase(smem_u32(&sh.p_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
+          const uint32_t full = smem_u32(&sh.p_full[sl.idx]);
+          mbar_arrive_expect_tx(full, F::kPBytes + ((F::kFp4 && p.scale_tma) ? F::kSBytes : 0));
+          pend_mask |= 1u << sl.idx;
+          pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
           const int prow = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
-          const int pbatch = OP == kDgrad ? ti.e : 0;
+          uint8_t* dst = ring_p + sl.idx * F::kPStageBytes;
           if (FMT == BSQ_BF16) {
-            tma_load_3d(smem_u32(stage_a(stage)), &tm_p, full, m0, prow, pbatch);
-            tma_load_3d(smem_u32(stage_a(stage) + kBoxBytes), &tm_p, full, m0 + 64, prow, pbatch);
+            tma_load_3d(smem_u32(dst), &tm_p, full, m0, prow, pbatch);
+            tma_load_3d(smem_u32(dst + kBoxBytes), &tm_p, full, m0 + 64, prow, pbatch);
           } else {
-            const int x = FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2;
-            tma_load_3d(smem_u32(stage_p(stage)), &tm_p, full, x, prow, pbatch);
+            tma_load_3d(smem_u32(dst), &tm_p, full, FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2, prow, pbatch);
             if (F::kFp4 && p.scale_tma) {
               // 16-byte aligned window holding this tile's scales (4 or 8 bytes per row)
               const int xs = (FMT == BSQ_MXFP4 ? (m0 >> 5) : (m0 >> 4)) & ~15;
-              tma_load_3d(smem_u32(stage_s(stage)), &tm_s, full, xs, prow, pbatch);
+              tma_load_3d(smem_u32(dst + F::kPBytes), &tm_s, full, xs, prow, pbatch);
             }
           }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) drain_pending<kPStages>(sh.p_full, pend_mask, pend_par, limit);
+    }
+  } else if (warp == 3) {
+    // ===== TMA producer: grad_out ring =====
+    if (lane == 0) {
+      uint32_t kc = 0;
+      int e_cur = 0;
+      uint32_t pend_mask = 0, pend_par = 0;
+      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+        const int nbox = (ti.n_valid + 63) >> 6;
+        bool ok = true;
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
+          const Slot sl = ring_slot<kBStages>(kc);
+          if (!wait_phase(smem_u32(&sh.b_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
+          const uint32_t full = smem_u32(&sh.b_full[sl.idx]);
+          mbar_arrive_expect_tx(full, nbox * kBoxBytes);
+          pend_mask |= 1u << sl.idx;
+          pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
+          uint8_t* dst = ring_b + sl.idx * kBBytes;
           for (int j = 0; j < nbox; ++j) {
             if (OP == kDgrad)
-              tma_load_2d(smem_u32(stage_b(stage) + j * kBoxBytes), &tm_g, full, kb * kTileK,
-                          ti.r0 + ti.nt * kTileN + 64 * j);
+              tma_load_2d(smem_u32(dst + j * kBoxBytes), &tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + 64 * j);
             else
-              tma_load_2d(smem_u32(stage_b(stage) + j * kBoxBytes), &tm_g, full, ti.nt * kTileN + 64 * j,
-                          ti.r0 + kb * kTileK);
+              tma_load_2d(smem_u32(dst + j * kBoxBytes), &tm_g, full, ti.nt * kTileN + 64 * j, ti.r0 + kb * kTileK);
           }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        if (!ok) break;
       }
-      if (*abort_flag) {
-        // Let every issued copy land before the CTA's shared memory is released.
-        for (int s = 0; s < kStages; ++s)
-          if (pend_mask & (1u << s)) {
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(smem_u32(&sh.full[s]), (pend_par >> s) & 1u) &&
-                   global_timer_ns() - t0 < limit) {
-            }
-          }
-      }
+      if (*abort_flag) drain_pending<kBStages>(sh.b_full, pend_mask, pend_par, limit);
     }
   } else if (warp == 1) {
     // ===== MMA issuer =====
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      uint32_t kc = 0;
       int e_cur = 0;
       uint32_t acc = 0;
       for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
@@ -311,11 +363,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(kTileM, n_mma, true, OP == kWgrad);
         const uint32_t d_tmem = tmem_base + buf * kTileN;
         bool ok = true;
-        for (int kb = 0; kb < ti.kblocks; ++kb) {
-          if (!wait_phase(smem_u32(&sh.ready[stage]), phase, abort_flag, p.err, limit)) { ok = false; break; }
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
+          const Slot sa = ring_slot<kAStages>(kc);
+          const Slot sb = ring_slot<kBStages>(kc);
+          if (!wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit) ||
+              !wait_phase(smem_u32(&sh.a_full[sa.idx]), sa.par, abort_flag, p.err, limit)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(stage_a(stage));
-          const uint32_t b_base = smem_u32(stage_b(stage));
+          const uint32_t a_base = smem_u32(ring_a + sa.idx * kABytes);
+          const uint32_t b_base = smem_u32(ring_b + sb.idx * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             // A: MN-major, swizzle columns of 64 m at 8 KB, 8-row groups at 1 KB; 16 k-rows = 2 KB.
@@ -327,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               bdesc = sdesc_sw128(b_base + kk * 2048, kBoxBytes, 1024);
             umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&sh.empty[stage]));
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          umma_commit(smem_u32(&sh.a_empty[sa.idx]));
+          umma_commit(smem_u32(&sh.b_empty[sb.idx]));
         }
         if (!ok) break;
         umma_commit(smem_u32(&sh.tmem_full[buf]));
@@ -393,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qtr = lane >> 3;
     const int r = dw * 8 + (qtr & 1) * 4 + (lane & 3);          // 0..63
     const int g = (qtr >> 1) * 2 + ((lane >> 2) & 1);           // 0..3
-    uint32_t kcount = 0;                                       // k-blocks seen so far (all teams)
+    uint32_t kc = 0;                                           // k-blocks seen so far (all teams)
     int e_cur = 0;
     for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
       const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
@@ -404,10 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float tscale = 0.f;
       if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + pbatch);
       bool ok = true;
-      for (int kb = 0; kb < ti.kblocks; ++kb, ++kcount) {
-        if (static_cast<int>(kcount % kDeqTeams) != team) continue;
-        const int stage = static_cast<int>(kcount % kStages);
-        const uint32_t phase = (kcount / kStages) & 1u;
+      for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
+        if (static_cast<int>(kc % kDeqTeams) != team) continue;
+        const Slot sp = ring_slot<kPStages>(kc);
+        const Slot sa = ring_slot<kAStages>(kc);
         const int prow0 = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
         const int kvalid = OP == kDgrad ? min(kTileK, p.N - kb * kTileK) : min(kTileK, ti.r1 - prow0);
         const bool valid = r < kvalid && col_ok;
@@ -425,77 +483,101 @@ __global__ void __launch_bounds__(kThreads, 1)
             sraw = static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4))) |
                    (static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
         }
-        ok = wait_phase(smem_u32(&sh.full[stage]), phase, abort_flag, p.err, limit);
+        ok = wait_phase(smem_u32(&sh.p_full[sp.idx]), sp.par, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        uint8_t* a_tile = stage_a(stage);
-        if (FMT != BSQ_BF16) {
-          uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
-          if (valid) {
-            const uint8_t* prow = stage_p(stage) + r * F::kPRowBytes;
-            if (F::kFp4) {
-              if (p.scale_tma) {
-                const uint8_t* srow = stage_s(stage) + r * 16;
-                if (FMT == BSQ_MXFP4)
-                  sraw = srow[((m0 >> 5) & 15) + g];
-                else
-                  sraw = *reinterpret_cast<const uint16_t*>(srow + ((m0 >> 4) & 15) + 2 * g);
-              }
-              const uint4 w = *reinterpret_cast<const uint4*>(prow + 16 * g);
-              ScaleBf16 s0, s1;
-              if (FMT == BSQ_MXFP4) {
-                s0 = make_scale_e8m0(sraw);
-                s1 = s0;
-              } else {
-                s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
-                s1 = make_scale_nvfp4(sraw >> 8, tscale);
-              }
-              decode_e2m1x8(w.x, s0, v[0]);
-              decode_e2m1x8(w.y, s0, v[1]);
-              decode_e2m1x8(w.z, s1, v[2]);
-              decode_e2m1x8(w.w, s1, v[3]);
-            } else {
-              // rows 128 bytes apart share banks: odd rows read their second half first
-              const int h = r & 1;
-              uint4 wa = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * h);
-              uint4 wb = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * (h ^ 1));
-              if (h) {
-                const uint4 t = wa;
-                wa = wb;
-                wb = t;
-              }
-              const ScaleBf16 s0 = make_scale_fp8(sf);
-              decode_e4m3x8(wa.x, wa.y, s0, v[0]);
-              decode_e4m3x8(wa.z, wa.w, s0, v[1]);
-              decode_e4m3x8(wb.x, wb.y, s0, v[2]);
-              decode_e4m3x8(wb.z, wb.w, s0, v[3]);
+        // ---- read this thread's packed bytes (and scale) out of the packed ring
+        const uint8_t* pst = ring_p + sp.idx * F::kPStageBytes;
+        uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
+        if (FMT != BSQ_BF16 && valid) {
+          const uint8_t* prow = pst + r * F::kPRowBytes;
+          if (F::kFp4) {
+            if (p.scale_tma) {
+              const uint8_t* srow = pst + F::kPBytes + r * 16;
+              if (FMT == BSQ_MXFP4)
+                sraw = srow[((m0 >> 5) & 15) + g];
+              else
+                sraw = *reinterpret_cast<const uint16_t*>(srow + ((m0 >> 4) & 15) + 2 * g);
             }
+            wa = *reinterpret_cast<const uint4*>(prow + 16 * g);
           } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) v[j][i] = 0u;
+            // rows 128 bytes apart share banks: odd rows read their second half first
+            const int h = r & 1;
+            wa = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * h);
+            wb = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * (h ^ 1));
+            if (h) {
+              const uint4 tmp = wa;
+              wa = wb;
+              wb = tmp;
+            }
           }
-          // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
-          // 16-byte slot (4(g&1) + j) XOR (r & 7)
-          uint8_t* rowp = a_tile + (g >> 1) * kBoxBytes + r * 128;
+        }
+        uint4 cp[4];
+        if (FMT == BSQ_BF16) {
+          // BF16 operand: the TMA tile is already in the swizzled layout; copy this
+          // thread's four 16-byte chunks (zero outside the contraction).
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int slot = ((g & 1) * 4 + j) ^ (r & 7);
-            *reinterpret_cast<uint4*>(rowp + (slot << 4)) = make_uint4(v[j][0], v[j][1], v[j][2], v[j][3]);
+            cp[j] = r < kvalid ? *reinterpret_cast<const uint4*>(pst + (g >> 1) * kBoxBytes + r * 128 + (slot << 4))
+                               : make_uint4(0, 0, 0, 0);
           }
-        } else if (kvalid < kTileK) {
-          // BF16 operand from TMA: zero the rows outside the contraction
-          const int dt = dw * 32 + lane;
-          for (int idx = dt; idx < (kTileK - kvalid) * 16; idx += 256) {
-            const int rr = kvalid + idx / 16, c = idx % 16;
-            *reinterpret_cast<uint4*>(a_tile + (c >> 3) * kBoxBytes + rr * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));   // packed slot free
+        // ---- decode into the BF16 operand ring
+        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
+        if (FMT == BSQ_BF16) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[j][0] = cp[j].x; v[j][1] = cp[j].y; v[j][2] = cp[j].z; v[j][3] = cp[j].w;
           }
+        } else if (valid) {
+          if (F::kFp4) {
+            ScaleBf16 s0, s1;
+            if (FMT == BSQ_MXFP4) {
+              s0 = make_scale_e8m0(sraw);
+              s1 = s0;
+            } else {
+              s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
+              s1 = make_scale_nvfp4(sraw >> 8, tscale);
+            }
+            decode_e2m1x8(wa.x, s0, v[0]);
+            decode_e2m1x8(wa.y, s0, v[1]);
+            decode_e2m1x8(wa.z, s1, v[2]);
+            decode_e2m1x8(wa.w, s1, v[3]);
+          } else {
+            const ScaleBf16 s0 = make_scale_fp8(sf);
+            decode_e4m3x8(wa.x, wa.y, s0, v[0]);
+            decode_e4m3x8(wa.z, wa.w, s0, v[1]);
+            decode_e4m3x8(wb.x, wb.y, s0, v[2]);
+            decode_e4m3x8(wb.z, wb.w, s0, v[3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[j][i] = 0u;
+        }
+        ok = wait_phase(smem_u32(&sh.a_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
+        // 16-byte slot (4(g&1) + j) XOR (r & 7)
+        uint8_t* rowp = ring_a + sa.idx * kABytes + (g >> 1) * kBoxBytes + r * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int slot = ((g & 1) * 4 + j) ^ (r & 7);
+          *reinterpret_cast<uint4*>(rowp + (slot << 4)) = make_uint4(v[j][0], v[j][1], v[j][2], v[j][3]);
         }
         if (OP == kWgrad && kvalid < kTileK) {
           // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must not
-          // reach the products: zero them in every loaded box.
-          uint8_t* b_tile = stage_b(stage);
+          // reach the products: zero them in every loaded box, once the boxes have landed.
+          const Slot sb = ring_slot<kBStages>(kc);
+          ok = wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          uint8_t* b_tile = ring_b + sb.idx * kBBytes;
           const int nbox = (ti.n_valid + 63) >> 6;
           const int dt = dw * 32 + lane;
           for (int idx = dt; idx < (kTileK - kvalid) * 8 * nbox; idx += 256) {
@@ -507,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.ready[stage]));
+        if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[sa.idx]));
       }
       if (!ok) break;
     }
@@ -629,7 +711,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   const int64_t bound = OP == kDgrad ? p.num_m * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_m * nn * a.E;
   int64_t grid = bound < a.num_sms ? bound : a.num_sms;
   if (grid < 1) grid = 1;
-  const size_t smem = static_cast<size_t>(F::kStages) * F::kStageBytes + sizeof(SharedTail) + 1024;
+  const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
   auto kern = bsq_gemm_kernel<FMT, OP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) {
