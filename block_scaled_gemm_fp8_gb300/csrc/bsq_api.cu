@@ -161,6 +161,7 @@ int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t 
   if (st != BSQ_OK) return st;
   return check_packed("bsq_linear_dgrad", w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, true);
 }
+int device_error_word(int32_t** err, int* sms) { return device_state(err, sms); }
 int set_error(int status, const char* message) {
   return fail(static_cast<bsq_status>(status), "%s", message);
 }
@@ -253,7 +254,7 @@ bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N, int32_t 
     st = workspace(bsq::smallm_workspace_bytes(K), static_cast<cudaStream_t>(stream), &ws);
     if (st != BSQ_OK) return st;
     bsq::SmallMArgs s{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, M, N, K, grad_x, ws, sms,
-                      static_cast<cudaStream_t>(stream)};
+                      static_cast<cudaStream_t>(stream), err};
     const char* msg = "";
     if (bsq::launch_smallm(s, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
     return BSQ_OK;

@@ -451,6 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qtr = lane >> 3;
     const int r = dw * 8 + (qtr & 1) * 4 + (lane & 3);          // 0..63
     const int g = (qtr >> 1) * 2 + ((lane >> 2) & 1);           // 0..3
+    // Shared addresses that do not change between k-blocks: the four swizzled 16-byte
+    // store slots of this thread inside an A stage, and its packed bytes inside a P stage.
+    const uint32_t a_ring = smem_u32(ring_a), p_ring = smem_u32(ring_p);
+    uint32_t st_off[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_off[j] = (g >> 1) * kBoxBytes + r * 128 + ((((g & 1) * 4 + j) ^ (r & 7)) << 4);
+    const uint32_t p_off = F::kFp4 ? r * F::kPRowBytes + 16 * g : r * F::kPRowBytes + 32 * g + 16 * (r & 1);
     uint32_t kc = 0;                                           // k-blocks seen so far (all teams)
     int e_cur = 0;
     for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
@@ -461,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pbatch = OP == kDgrad ? ti.e : 0;
       float tscale = 0.f;
       if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + pbatch);
+      // this thread's scale byte(s) inside the staged 16-byte scale window of a row
+      const uint32_t s_off = F::kPBytes + r * 16 + (FMT == BSQ_MXFP4 ? ((m0 >> 5) & 15) + g : ((m0 >> 4) & 15) + 2 * g);
       bool ok = true;
       for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
         if (static_cast<int>(kc % kDeqTeams) != team) continue;
@@ -469,11 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int prow0 = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
         const int kvalid = OP == kDgrad ? min(kTileK, p.N - kb * kTileK) : min(kTileK, ti.r1 - prow0);
         const bool valid = r < kvalid && col_ok;
-        const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + r;
         // Scales that do not come through TMA are fetched before the wait.
         uint32_t sraw = 0;
         float sf = 0.f;
         if (valid) {
+          const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + r;
           if (FMT == BSQ_FP8_E4M3_B128)
             sf = __ldg(reinterpret_cast<const float*>(p.scale) +
                        (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + r) >> 7)) * p.scale_ld + (col0 >> 7));
@@ -487,89 +497,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         // ---- read this thread's packed bytes (and scale) out of the packed ring
-        const uint8_t* pst = ring_p + sp.idx * F::kPStageBytes;
+        const uint32_t pst = p_ring + sp.idx * F::kPStageBytes;
         uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
         if (FMT != BSQ_BF16 && valid) {
-          const uint8_t* prow = pst + r * F::kPRowBytes;
           if (F::kFp4) {
-            if (p.scale_tma) {
-              const uint8_t* srow = pst + F::kPBytes + r * 16;
-              if (FMT == BSQ_MXFP4)
-                sraw = srow[((m0 >> 5) & 15) + g];
-              else
-                sraw = *reinterpret_cast<const uint16_t*>(srow + ((m0 >> 4) & 15) + 2 * g);
-            }
-            wa = *reinterpret_cast<const uint4*>(prow + 16 * g);
+            if (p.scale_tma) sraw = FMT == BSQ_MXFP4 ? lds_u8(pst + s_off) : lds_u16(pst + s_off);
+            wa = lds128(pst + p_off);
           } else {
             // rows 128 bytes apart share banks: odd rows read their second half first
-            const int h = r & 1;
-            wa = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * h);
-            wb = *reinterpret_cast<const uint4*>(prow + 32 * g + 16 * (h ^ 1));
-            if (h) {
+            wa = lds128(pst + p_off);
+            wb = lds128(pst + (p_off ^ 16u));
+            if (r & 1) {
               const uint4 tmp = wa;
               wa = wb;
               wb = tmp;
             }
           }
         }
-        uint4 cp[4];
+        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
         if (FMT == BSQ_BF16) {
           // BF16 operand: the TMA tile is already in the swizzled layout; copy this
           // thread's four 16-byte chunks (zero outside the contraction).
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int slot = ((g & 1) * 4 + j) ^ (r & 7);
-            cp[j] = r < kvalid ? *reinterpret_cast<const uint4*>(pst + (g >> 1) * kBoxBytes + r * 128 + (slot << 4))
-                               : make_uint4(0, 0, 0, 0);
+            const uint4 c = r < kvalid ? lds128(pst + st_off[j]) : make_uint4(0, 0, 0, 0);
+            v[j][0] = c.x; v[j][1] = c.y; v[j][2] = c.z; v[j][3] = c.w;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));   // packed slot free
         // ---- decode into the BF16 operand ring
-        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
-        if (FMT == BSQ_BF16) {
+        if (FMT != BSQ_BF16) {
+          if (valid) {
+            if (F::kFp4) {
+              spread_e2m1x8(wa.x, v[0]);
+              spread_e2m1x8(wa.y, v[1]);
+              spread_e2m1x8(wa.z, v[2]);
+              spread_e2m1x8(wa.w, v[3]);
+              ScaleBf16 s0, s1;
+              if (FMT == BSQ_MXFP4) {
+                s0 = make_scale_e8m0(sraw);
+                s1 = s0;
+              } else {
+                s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
+                s1 = make_scale_nvfp4(sraw >> 8, tscale);
+              }
+              if (s0.fast && s1.fast) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[j][0] = cp[j].x; v[j][1] = cp[j].y; v[j][2] = cp[j].z; v[j][3] = cp[j].w;
-          }
-        } else if (valid) {
-          if (F::kFp4) {
-            ScaleBf16 s0, s1;
-            if (FMT == BSQ_MXFP4) {
-              s0 = make_scale_e8m0(sraw);
-              s1 = s0;
+                for (int i = 0; i < 4; ++i) {
+                  v[0][i] = bf16x2_mul(v[0][i], s0.c2);
+                  v[1][i] = bf16x2_mul(v[1][i], s0.c2);
+                  v[2][i] = bf16x2_mul(v[2][i], s1.c2);
+                  v[3][i] = bf16x2_mul(v[3][i], s1.c2);
+                }
+              } else {
+                scale_pairs4(v[0], s0, kPow2_126x2);
+                scale_pairs4(v[1], s0, kPow2_126x2);
+                scale_pairs4(v[2], s1, kPow2_126x2);
+                scale_pairs4(v[3], s1, kPow2_126x2);
+              }
             } else {
-              s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
-              s1 = make_scale_nvfp4(sraw >> 8, tscale);
+              const ScaleBf16 s0 = make_scale_fp8(sf);
+              decode_e4m3x8(wa.x, wa.y, s0, v[0]);
+              decode_e4m3x8(wa.z, wa.w, s0, v[1]);
+              decode_e4m3x8(wb.x, wb.y, s0, v[2]);
+              decode_e4m3x8(wb.z, wb.w, s0, v[3]);
             }
-            decode_e2m1x8(wa.x, s0, v[0]);
-            decode_e2m1x8(wa.y, s0, v[1]);
-            decode_e2m1x8(wa.z, s1, v[2]);
-            decode_e2m1x8(wa.w, s1, v[3]);
           } else {
-            const ScaleBf16 s0 = make_scale_fp8(sf);
-            decode_e4m3x8(wa.x, wa.y, s0, v[0]);
-            decode_e4m3x8(wa.z, wa.w, s0, v[1]);
-            decode_e4m3x8(wb.x, wb.y, s0, v[2]);
-            decode_e4m3x8(wb.z, wb.w, s0, v[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[j][i] = 0u;
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[j][i] = 0u;
         }
         ok = wait_phase(smem_u32(&sh.a_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
         // 16-byte slot (4(g&1) + j) XOR (r & 7)
-        uint8_t* rowp = ring_a + sa.idx * kABytes + (g >> 1) * kBoxBytes + r * 128;
+        const uint32_t ast = a_ring + sa.idx * kABytes;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int slot = ((g & 1) * 4 + j) ^ (r & 7);
-          *reinterpret_cast<uint4*>(rowp + (slot << 4)) = make_uint4(v[j][0], v[j][1], v[j][2], v[j][3]);
-        }
+        for (int j = 0; j < 4; ++j) sts128(ast + st_off[j], v[j][0], v[j][1], v[j][2], v[j][3]);
         if (OP == kWgrad && kvalid < kTileK) {
           // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must not
           // reach the products: zero them in every loaded box, once the boxes have landed.
@@ -577,14 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          uint8_t* b_tile = ring_b + sb.idx * kBBytes;
+          const uint32_t b_tile = smem_u32(ring_b + sb.idx * kBBytes);
           const int nbox = (ti.n_valid + 63) >> 6;
           const int dt = dw * 32 + lane;
           for (int idx = dt; idx < (kTileK - kvalid) * 8 * nbox; idx += 256) {
             const int box = idx / ((kTileK - kvalid) * 8);
             const int rem = idx % ((kTileK - kvalid) * 8);
             const int rr = kvalid + rem / 8, c = rem % 8;
-            *reinterpret_cast<uint4*>(b_tile + box * kBoxBytes + rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            sts128(b_tile + box * kBoxBytes + rr * 128 + c * 16, 0u, 0u, 0u, 0u);
           }
         }
         fence_proxy_async_smem();
@@ -624,6 +632,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+// Tiled tensor map through the driver entry point (no link against libcuda); also used by
+// the small-M kernel.
 bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* base, const uint64_t* dims,
                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
   auto fn = get_encode_fn();
@@ -633,6 +645,8 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const voi
                         sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int FMT, int OP>
 int launch_typed(const GemmArgs& a, const char** msg) {

@@ -66,6 +66,7 @@ struct SmallMArgs {
   void* ws;               // FP32 workspace of smallm_workspace_bytes(K) bytes, zero between calls
   int num_sms;
   cudaStream_t stream;
+  int32_t* err;           // device error word
 };
 
 constexpr int kSmallM = 16;  // dgrad with at most this many rows takes the split-K kernel
@@ -75,6 +76,8 @@ int launch_smallm(const SmallMArgs& a, const char** msg);
 // Host-side argument checks of bsq_linear_dgrad (bsq_api.cu); BSQ_OK when well formed.
 int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
                             const void* w_scale, const float* w_tensor_scale, int64_t K, const void* grad_x);
+// The current device's error word and SM count (no allocation); BSQ_OK on success.
+int device_error_word(int32_t** err, int* sms);
 // Record a message for bsq_last_error() and return `status`.
 int set_error(int status, const char* message);
 

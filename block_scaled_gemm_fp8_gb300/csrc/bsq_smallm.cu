@@ -4,26 +4,32 @@
 // With M this small the product is bound by reading the packed weight once from HBM, so
 // the kernel is shaped for bandwidth, not for the tensor-core peak:
 //   * split-K over the N rows of W: every CTA owns a 128-column slab of K and a range of
-//     rows, so the whole GPU streams W concurrently (two CTAs per SM);
-//   * the packed bytes go straight from global memory into registers (64-byte contiguous
-//     row segments per load instruction) and are decoded there -- no shared-memory staging
-//     of the BF16 weight;
+//     up to 512 rows, so that about two CTAs per SM cover W in one wave;
+//   * one thread stages the CTA's whole W slab, its scale slab and the matching grad_out
+//     slab into shared memory with TMA behind a single barrier, so all of W is in flight
+//     at once and the kernel runs at memory speed rather than at memory latency;
 //   * decoding pairs the same column of two adjacent rows in one 32-bit register
 //     (one byte permute + the multiply-spread of bsq_decode.cuh), which is exactly the
-//     k-pair an mma.sync B fragment wants, so no transpose is needed;
+//     k-pair an mma.sync B fragment wants, so no transpose and no BF16 staging is needed;
 //   * m16n8k16 BF16 mma.sync with FP32 accumulators (tokens are the M=16 side);
-//   * the CTAs of a slab reduce through an FP32 workspace with atomics; the last CTA to
-//     finish a slab converts it to BF16, writes grad_X and zeroes the workspace again.
+//   * the warps of a CTA reduce through shared memory, the CTAs of a slab through an FP32
+//     workspace with 16-byte reduction atomics; the last CTA to finish a slab converts it
+//     to BF16, writes grad_X and zeroes the workspace again.
 #include <cstdio>
 #include <mutex>
 
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include "bsq_decode.cuh"
 #include "bsq_internal.h"
+#include "bsq_ptx.cuh"
 #include "../../include/bsq.h"
 
 namespace bsq {
+
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* base, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
 
 namespace {
 
@@ -32,18 +38,34 @@ constexpr int kThreadsSm = kWarps * 32;
 constexpr int kSlab = 128;       // columns of K per CTA
 constexpr int kStep = 16;        // rows of N per mma k-step
 constexpr int kNT = 16;          // n-tiles (8 columns each) per warp per k-step
+constexpr int kMaxRows = 512;    // rows of W per CTA
+constexpr int kBox = 256;        // rows per TMA box
 
 struct SmallParams {
-  const __nv_bfloat16* g;
-  const uint8_t* w;
   const uint8_t* scale;
   const float* tensor_scale;
   __nv_bfloat16* out;
   float* ws;          // [16][K] FP32, all zero between calls
   int32_t* counters;  // [num_slabs], all zero between calls
   int32_t M, N, K;
-  int32_t rows_per_split;
-  int32_t scale_ld;   // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128)
+  int32_t rows_per_split;   // multiple of kStep * kWarps, <= kMaxRows
+  int32_t scale_ld;         // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128)
+  int32_t scale_tma;        // FP4 scale slab through TMA
+  uint64_t timeout_ns;
+  int32_t* err;
+};
+
+template <int FMT>
+struct SmallFmt {
+  static constexpr int kRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2;
+  static constexpr int kWBytes = kMaxRows * kRowBytes;
+  static constexpr int kSBytes = FMT == BSQ_FP8_E4M3_B128 ? 0 : kMaxRows * 16;
+  static constexpr int kGBytes = 16 * kMaxRows * 2;
+  static constexpr int kRedBytes = kWarps * kNT * 16 * 8 * 4;   // per-warp partial slabs
+  static constexpr int kStageBytes = kWBytes + kSBytes + kGBytes;
+  // staged slabs (later reused for the partials), the summed slab, the barrier and the flag;
+  // plus 1 KB to align the base for the 128-byte swizzled grad_out boxes
+  static constexpr int kSmem = (kStageBytes > kRedBytes ? kStageBytes : kRedBytes) + 16 * kSlab * 4 + 128 + 1024;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -52,6 +74,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 // Scale pair for two rows: (s_a, s_b) with the combined fast path only when both are exact.
@@ -73,133 +100,56 @@ __device__ __forceinline__ uint32_t pair_bytes(uint32_t x, uint32_t y, int b) {
 }
 
 template <int FMT>
-struct RowData;  // packed bytes of one thread's 16 columns in one row
-
-template <>
-struct RowData<BSQ_MXFP4> { uint2 v; };
-template <>
-struct RowData<BSQ_NVFP4> { uint2 v; };
-template <>
-struct RowData<BSQ_FP8_E4M3_B128> { uint4 v; };
-
-template <int FMT>
-__device__ __forceinline__ void load_row(RowData<FMT>& d, const SmallParams& p, int row, int col, bool ok) {
-  if (FMT == BSQ_FP8_E4M3_B128) {
-    uint4 z = make_uint4(0, 0, 0, 0);
-    if (ok) z = __ldg(reinterpret_cast<const uint4*>(p.w + static_cast<int64_t>(row) * p.K + col));
-    reinterpret_cast<uint4&>(d.v) = z;
-  } else {
-    uint2 z = make_uint2(0, 0);
-    if (ok) z = __ldg(reinterpret_cast<const uint2*>(p.w + static_cast<int64_t>(row) * (p.K / 2) + col / 2));
-    reinterpret_cast<uint2&>(d.v) = z;
-  }
-}
-
-// One k-step worth of raw inputs of this thread: rows (a,b) feed B register 0, rows (c,d) register 1.
-template <int FMT>
-struct StepData {
-  RowData<FMT> r[4];
-  uint32_t sraw[4];   // FP4: scale byte per row
-  float sf;           // FP8: block scale (all four rows share one 128-row block)
-};
-
-template <int FMT>
-__device__ __forceinline__ void load_step(StepData<FMT>& s, const SmallParams& p, int base, int q, int col,
-                                          bool col_ok, int n1) {
-  const int rows[4] = {base + 2 * q, base + 2 * q + 1, base + 8 + 2 * q, base + 9 + 2 * q};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool ok = col_ok && rows[i] < n1;
-    load_row<FMT>(s.r[i], p, rows[i], col, ok);
-    s.sraw[i] = 0;
-    if (FMT == BSQ_MXFP4 && ok) s.sraw[i] = __ldg(p.scale + static_cast<int64_t>(rows[i]) * p.scale_ld + (col >> 5));
-    if (FMT == BSQ_NVFP4 && ok) s.sraw[i] = __ldg(p.scale + static_cast<int64_t>(rows[i]) * p.scale_ld + (col >> 4));
-  }
-  s.sf = 0.f;
-  if (FMT == BSQ_FP8_E4M3_B128 && col_ok && base < n1)
-    s.sf = __ldg(reinterpret_cast<const float*>(p.scale) + static_cast<int64_t>(base >> 7) * p.scale_ld + (col >> 7));
-}
-
-template <int FMT>
 __device__ __forceinline__ ScaleBf16 row_scale(uint32_t raw, float tscale) {
   if (FMT == BSQ_MXFP4) return make_scale_e8m0(raw);
   return make_scale_nvfp4(raw, tscale);
 }
 
-// Decode part `wi` of one k-step into B fragments for n-tiles [kPart*wi, kPart*(wi+1)):
-// b0[i] from rows (a,b), b1[i] from rows (c,d).  FP4: 2 parts of 8 n-tiles (one packed
-// word per row each); FP8: 4 parts of 4 n-tiles.
 template <int FMT>
-struct Part {
-  static constexpr int kParts = FMT == BSQ_FP8_E4M3_B128 ? 4 : 2;
-  static constexpr int kTiles = kNT / kParts;
-};
-
-template <int FMT>
-__device__ __forceinline__ void decode_part(const StepData<FMT>& s, float tscale, int wi,
-                                            uint32_t (&b0)[Part<FMT>::kTiles], uint32_t (&b1)[Part<FMT>::kTiles]) {
-  if (FMT == BSQ_FP8_E4M3_B128) {
-    const ScaleBf16 sc = make_scale_fp8(s.sf);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t* xw = reinterpret_cast<const uint32_t*>(&s.r[2 * half].v);
-      const uint32_t* yw = reinterpret_cast<const uint32_t*>(&s.r[2 * half + 1].v);
-      uint32_t(&dst)[Part<FMT>::kTiles] = half ? b1 : b0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t v = pair_bytes(xw[wi], yw[wi], j);   // column 4wi+j of both rows
-        uint32_t o = scale_one(((v << 4) & 0x07F007F0u) | ((v << 8) & 0x80008000u), sc, kPow2_120x2);
-        if ((v & 0x7Fu) == 0x7Fu) o = (o & 0xFFFF0000u) | kBf16NaN;             // E4M3 NaN, first row
-        if ((v & 0x007F0000u) == 0x007F0000u) o = (o & 0xFFFFu) | (kBf16NaN << 16);  // second row
-        dst[j] = o;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t* xw = reinterpret_cast<const uint32_t*>(&s.r[2 * half].v);
-      const uint32_t* yw = reinterpret_cast<const uint32_t*>(&s.r[2 * half + 1].v);
-      const ScaleBf16 sc = pair_scales(row_scale<FMT>(s.sraw[2 * half], tscale),
-                                       row_scale<FMT>(s.sraw[2 * half + 1], tscale));
-      uint32_t(&dst)[Part<FMT>::kTiles] = half ? b1 : b0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t v = pair_bytes(xw[wi], yw[wi], j);          // byte 4wi+j of both rows
-        const uint32_t lo = ((v & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;   // column 8wi+2j
-        const uint32_t hi = ((v & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;   // column 8wi+2j+1
-        dst[2 * j] = scale_one(lo, sc, kPow2_126x2);
-        dst[2 * j + 1] = scale_one(hi, sc, kPow2_126x2);
-      }
-    }
-  }
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(kThreadsSm, 2) smallm_dgrad_kernel(const SmallParams p) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
+__global__ void __launch_bounds__(kThreadsSm, 2)
+    smallm_dgrad_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+                        const __grid_constant__ CUtensorMap tm_g, const SmallParams p) {
+  using F = SmallFmt<FMT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kStaged = F::kStageBytes > F::kRedBytes ? F::kStageBytes : F::kRedBytes;
+  uint8_t* ws_w = base;                               // [rows][kRowBytes] packed W
+  uint8_t* ws_s = ws_w + F::kWBytes;                  // [rows][16] FP4 scale windows
+  uint8_t* ws_g = ws_s + F::kSBytes;                  // [rows/64][16 tokens][64] BF16 grad_out, 128B-swizzled
+  float* red = reinterpret_cast<float*>(base);        // reused after the main loop
+  float* red_sum = reinterpret_cast<float*>(base + kStaged);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + kStaged + 16 * kSlab * 4);
+  int* last_flag = reinterpret_cast<int*>(base + kStaged + 16 * kSlab * 4 + 64);
   const int slab = blockIdx.x;
   const int cb = slab * kSlab;
   const int n0 = blockIdx.y * p.rows_per_split;
   const int n1 = min(p.N, n0 + p.rows_per_split);
   const int nrows = max(n1 - n0, 0);
-  const int pitch = p.rows_per_split + 8;   // bf16 elements per token row of the G slab (16-byte skew)
-  __nv_bfloat16* gs = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-  float* red = reinterpret_cast<float*>(smem_raw + static_cast<size_t>(16) * pitch * 2);
-  __shared__ int last_flag;
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
 
-  // grad_out slab [16 tokens][rows] (zero past M or past the row range) and the reduction buffer
-  for (int i = tid; i < 16 * (pitch / 2); i += kThreadsSm) {
-    const int t = i / (pitch / 2), c2 = (i % (pitch / 2)) * 2;
-    uint32_t v = 0;
-    if (t < p.M && c2 < nrows)  // nrows is even: N % 8 == 0 and n0 % 16 == 0
-      v = __ldg(reinterpret_cast<const uint32_t*>(p.g + static_cast<int64_t>(t) * p.N + n0 + c2));
-    reinterpret_cast<uint32_t*>(gs)[t * (pitch / 2) + c2 / 2] = v;
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    fence_mbar_init();
   }
   __syncthreads();
-
+  if (tid == 0) {
+    const int nbox = (nrows + kBox - 1) / kBox;
+    const int ngbox = (nrows + 63) / 64;
+    uint32_t bytes = nbox * kBox * F::kRowBytes + ngbox * 16 * 64 * 2;
+    if (F::kSBytes && p.scale_tma) bytes += nbox * kBox * 16;
+    mbar_arrive_expect_tx(smem_u32(bar), bytes);
+    for (int b = 0; b < nbox; ++b) {
+      const int row = n0 + b * kBox;
+      tma_load_2d(smem_u32(ws_w + b * kBox * F::kRowBytes), &tm_w, smem_u32(bar),
+                  FMT == BSQ_FP8_E4M3_B128 ? cb : cb / 2, row);
+      if (F::kSBytes && p.scale_tma)
+        tma_load_2d(smem_u32(ws_s + b * kBox * 16), &tm_s, smem_u32(bar),
+                    (FMT == BSQ_MXFP4 ? (cb >> 5) : (cb >> 4)) & ~15, row);
+    }
+    for (int b = 0; b < ngbox; ++b)   // [16 tokens][64 rows] per box, 16-byte chunks XOR-swizzled by token
+      tma_load_2d(smem_u32(ws_g + b * 16 * 64 * 2), &tm_g, smem_u32(bar), n0 + 64 * b, 0);
+  }
   float tscale = 0.f;
   if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale);
   const int col = cb + 16 * g;
@@ -208,34 +158,105 @@ __global__ void __launch_bounds__(kThreadsSm, 2) smallm_dgrad_kernel(const Small
 #pragma unroll
   for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-  const int nsteps = (nrows + kStep - 1) / kStep;
-  StepData<FMT> cur, nxt;
-  int ks = warp;
-  if (ks < nsteps) load_step<FMT>(cur, p, n0 + ks * kStep, q, col, col_ok, n1);
-  for (; ks < nsteps; ks += kWarps) {
-    const int ks2 = ks + kWarps;
-    if (ks2 < nsteps) load_step<FMT>(nxt, p, n0 + ks2 * kStep, q, col, col_ok, n1);
-    // A fragment: grad_out[token][k] for k = local rows ks*16 .. +15
-    const uint32_t* g32 = reinterpret_cast<const uint32_t*>(gs);
-    const int k0 = ks * kStep;
-    uint32_t a[4];
-    a[0] = g32[g * (pitch / 2) + (k0 + 2 * q) / 2];
-    a[1] = g32[(g + 8) * (pitch / 2) + (k0 + 2 * q) / 2];
-    a[2] = g32[g * (pitch / 2) + (k0 + 8 + 2 * q) / 2];
-    a[3] = g32[(g + 8) * (pitch / 2) + (k0 + 8 + 2 * q) / 2];
-#pragma unroll
-    for (int wi = 0; wi < Part<FMT>::kParts; ++wi) {
-      uint32_t b0[Part<FMT>::kTiles], b1[Part<FMT>::kTiles];
-      decode_part<FMT>(cur, tscale, wi, b0, b1);
-#pragma unroll
-      for (int i = 0; i < Part<FMT>::kTiles; ++i) mma_bf16_16816(acc[wi * Part<FMT>::kTiles + i], a, b0[i], b1[i]);
+  // bounded wait for the slab
+  bool ok = true;
+  {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_sleep(smem_u32(bar), 0, 20000u)) {
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        ok = false;
+        break;
+      }
     }
-    if (ks2 < nsteps) cur = nxt;
   }
+  if (!ok) {
+    if (tid == 0) atomicCAS(p.err, 0, BSQ_DEVERR_TIMEOUT);
+  } else {
+    const int nsteps = (nrows + kStep - 1) / kStep;
+    for (int ks = warp; ks < nsteps; ks += kWarps) {
+      const int lr = ks * kStep;               // local row of this k-step
+      const int rows[4] = {lr + 2 * q, lr + 2 * q + 1, lr + 8 + 2 * q, lr + 9 + 2 * q};
+      // A fragment: grad_out[token][k] for k = local rows lr .. lr+15, read from the swizzled
+      // boxes ([16 tokens][64 rows], chunk of 8 rows XOR token & 7): conflict-free
+      const uint32_t gb = smem_u32(ws_g + (lr >> 6) * 16 * 64 * 2);
+      const int kl = lr & 63;                     // multiple of 16: chunks kl/8 and kl/8 + 1
+      const uint32_t c0 = static_cast<uint32_t>(((kl >> 3) ^ (g & 7)) << 4);
+      const uint32_t c1 = static_cast<uint32_t>((((kl >> 3) + 1) ^ (g & 7)) << 4);
+      uint32_t a[4];
+      a[0] = lds_u32(gb + g * 128 + c0 + 4 * q);
+      a[1] = lds_u32(gb + (g + 8) * 128 + c0 + 4 * q);
+      a[2] = lds_u32(gb + g * 128 + c1 + 4 * q);
+      a[3] = lds_u32(gb + (g + 8) * 128 + c1 + 4 * q);
+      if (FMT == BSQ_FP8_E4M3_B128) {
+        float sf = 0.f;
+        if (col_ok && n0 + lr < n1)
+          sf = __ldg(reinterpret_cast<const float*>(p.scale) + static_cast<int64_t>((n0 + lr) >> 7) * p.scale_ld + (col >> 7));
+        const ScaleBf16 sc = make_scale_fp8(sf);
+        uint4 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(ws_w + rows[i] * F::kRowBytes + 16 * g);
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          uint32_t b0[4], b1[4];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+            const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+            uint32_t(&dst)[4] = half ? b1 : b0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t v = pair_bytes(xw[wi], yw[wi], j);   // column 4wi+j of both rows
+              uint32_t o = scale_one(((v << 4) & 0x07F007F0u) | ((v << 8) & 0x80008000u), sc, kPow2_120x2);
+              if ((v & 0x7Fu) == 0x7Fu) o = (o & 0xFFFF0000u) | kBf16NaN;                 // E4M3 NaN, first row
+              if ((v & 0x007F0000u) == 0x007F0000u) o = (o & 0xFFFFu) | (kBf16NaN << 16);  // second row
+              dst[j] = o;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma_bf16_16816(acc[4 * wi + j], a, b0[j], b1[j]);
+        }
+      } else {
+        uint2 w[4];
+        uint32_t sraw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w[i] = *reinterpret_cast<const uint2*>(ws_w + rows[i] * F::kRowBytes + 8 * g);
+          const int grow = n0 + rows[i];
+          if (p.scale_tma) {
+            sraw[i] = FMT == BSQ_MXFP4 ? ws_s[rows[i] * 16 + ((cb >> 5) & 15) + (g >> 1)]
+                                       : ws_s[rows[i] * 16 + ((cb >> 4) & 15) + g];
+          } else {
+            sraw[i] = 0;
+            if (col_ok && grow < n1)
+              sraw[i] = __ldg(p.scale + static_cast<int64_t>(grow) * p.scale_ld + (FMT == BSQ_MXFP4 ? (col >> 5) : (col >> 4)));
+          }
+        }
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+          uint32_t b0[8], b1[8];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+            const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+            const ScaleBf16 sc = pair_scales(row_scale<FMT>(sraw[2 * half], tscale), row_scale<FMT>(sraw[2 * half + 1], tscale));
+            uint32_t(&dst)[8] = half ? b1 : b0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t v = pair_bytes(xw[wi], yw[wi], j);                   // byte 4wi+j of both rows
+              dst[2 * j] = scale_one(((v & 0x000F000Fu) * 0x1040u) & 0x81C081C0u, sc, kPow2_126x2);     // column 8wi+2j
+              dst[2 * j + 1] = scale_one(((v & 0x00F000F0u) * 0x0104u) & 0x81C081C0u, sc, kPow2_126x2);  // 8wi+2j+1
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mma_bf16_16816(acc[8 * wi + j], a, b0[j], b1[j]);
+        }
+      }
+    }
+  }
+  __syncthreads();   // everyone is done with the staged slabs; reuse them for the partials
 
-  // Cross-warp reduction through per-warp slabs laid out [nt][token][n] (8-byte stores of
-  // fragment column pairs, no bank conflicts); fragment column n of n-tile nt is output
-  // column cb + 16 n + nt.
+  // Per-warp partial slabs laid out [nt][token][n] (8-byte stores of fragment column pairs);
+  // fragment column n of n-tile nt is output column cb + 16 n + nt.
   {
     float* mine = red + warp * (kNT * 16 * 8);
 #pragma unroll
@@ -245,41 +266,48 @@ __global__ void __launch_bounds__(kThreadsSm, 2) smallm_dgrad_kernel(const Small
     }
   }
   __syncthreads();
-  // thread i sums the 8 warps for slab entries i, i + 256, ... (entry = (nt, token, n))
-  for (int i = tid; i < kNT * 16 * 8; i += kThreadsSm) {
+  // Sum the warps into red_sum laid out [token][128 columns]; entries are read in their
+  // own order (conflict-free) and scattered: entry (nt, token t, n) -> column 16 n + nt.
+  for (int e = tid; e < 16 * kSlab; e += kThreadsSm) {
+    const int n = e & 7, t = (e >> 3) & 15, nt = e >> 7;
     float v = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < kWarps; ++w2) v += red[w2 * (kNT * 16 * 8) + i];
-    red[kWarps * (kNT * 16 * 8) + i] = v;
+    for (int w2 = 0; w2 < kWarps; ++w2) v += red[w2 * (kNT * 16 * 8) + e];
+    red_sum[t * kSlab + 16 * n + nt] = v;
   }
   __syncthreads();
-  red += kWarps * (kNT * 16 * 8);   // reduced slab, same layout
-  // entry i = (nt, token t, fragment column n) holds output (t, cb + 16 n + nt); walking
-  // i = t*128 + c_local order keeps the global accesses coalesced.
-  auto entry = [](int t, int cl) { return ((cl & 15) * 16 + t) * 8 + (cl >> 4); };
+
   if (gridDim.y == 1) {
     for (int i = tid; i < 16 * kSlab; i += kThreadsSm) {
-      const int t = i / kSlab, cl = i % kSlab, c = cb + cl;
-      if (t < p.M && c < p.K) p.out[static_cast<int64_t>(t) * p.K + c] = __float2bfloat16_rn(red[entry(t, cl)]);
+      const int t = i / kSlab, c = cb + i % kSlab;
+      if (t < p.M && c < p.K) p.out[static_cast<int64_t>(t) * p.K + c] = __float2bfloat16_rn(red_sum[i]);
     }
     return;
   }
-  for (int i = tid; i < 16 * kSlab; i += kThreadsSm) {
-    const int t = i / kSlab, cl = i % kSlab, c = cb + cl;
-    if (t < p.M && c < p.K) atomicAdd(p.ws + static_cast<int64_t>(t) * p.K + c, red[entry(t, cl)]);
+  // 16-byte reduction atomics into the workspace (K % 16 == 0 keeps them aligned)
+  for (int i = tid; i < 16 * kSlab / 4; i += kThreadsSm) {
+    const int t = (4 * i) / kSlab, c = cb + (4 * i) % kSlab;
+    if (t < p.M && c < p.K)
+      red_add_v4(p.ws + static_cast<int64_t>(t) * p.K + c, red_sum[4 * i], red_sum[4 * i + 1], red_sum[4 * i + 2],
+                 red_sum[4 * i + 3]);
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) last_flag = (atomicAdd(p.counters + slab, 1) == static_cast<int>(gridDim.y) - 1);
+  if (tid == 0) *last_flag = (atomicAdd(p.counters + slab, 1) == static_cast<int>(gridDim.y) - 1);
   __syncthreads();
-  if (!last_flag) return;
+  if (!*last_flag) return;
   __threadfence();
-  for (int i = tid; i < 16 * kSlab; i += kThreadsSm) {
-    const int t = i / kSlab, c = cb + i % kSlab;
+  for (int i = tid; i < 16 * kSlab / 4; i += kThreadsSm) {
+    const int t = (4 * i) / kSlab, c = cb + (4 * i) % kSlab;
     if (t < p.M && c < p.K) {
-      float* w = p.ws + static_cast<int64_t>(t) * p.K + c;
-      p.out[static_cast<int64_t>(t) * p.K + c] = __float2bfloat16_rn(__ldcg(w));
-      __stcg(w, 0.f);
+      float4* w = reinterpret_cast<float4*>(p.ws + static_cast<int64_t>(t) * p.K + c);
+      const float4 v = __ldcg(w);
+      __stcg(w, make_float4(0.f, 0.f, 0.f, 0.f));
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(p.out + static_cast<int64_t>(t) * p.K + c) = pk;
     }
   }
   if (tid == 0) p.counters[slab] = 0;
@@ -294,25 +322,24 @@ size_t smallm_workspace_bytes(int64_t K) {
 
 int launch_smallm(const SmallMArgs& a, const char** msg) {
   SmallParams p;
-  p.g = static_cast<const __nv_bfloat16*>(a.g);
-  p.w = static_cast<const uint8_t*>(a.w_data);
   p.scale = static_cast<const uint8_t*>(a.w_scale);
   p.tensor_scale = a.w_tensor_scale;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.M = static_cast<int32_t>(a.M);
   p.N = static_cast<int32_t>(a.N);
   p.K = static_cast<int32_t>(a.K);
+  p.err = a.err;
+  p.timeout_ns = wait_limit_ns();
   p.scale_ld = a.fmt == BSQ_MXFP4 ? static_cast<int32_t>(a.K / 32)
                : a.fmt == BSQ_NVFP4 ? static_cast<int32_t>(a.K / 16)
                                     : static_cast<int32_t>((a.K + 127) / 128);
   const int slabs = static_cast<int>((a.K + kSlab - 1) / kSlab);
-  // about two CTAs per SM in one wave, at most 1024 rows of W per CTA
-  int splits = (2 * a.num_sms + slabs - 1) / slabs;
+  // about two CTAs per SM in one wave; rows per CTA a multiple of 128, at most 512
+  int splits = (2 * a.num_sms) / slabs;
   splits = splits < 1 ? 1 : splits;
   int rps = static_cast<int>((a.N + splits - 1) / splits);
-  rps = (rps + kStep - 1) / kStep * kStep;
-  if (rps > 1024) rps = 1024;
-  if (rps < kStep) rps = kStep;
+  rps = (rps + kStep * kWarps - 1) / (kStep * kWarps) * (kStep * kWarps);
+  if (rps > kMaxRows) rps = kMaxRows;
   splits = static_cast<int>((a.N + rps - 1) / rps);
   p.rows_per_split = rps;
   p.ws = static_cast<float*>(a.ws);
@@ -321,29 +348,59 @@ int launch_smallm(const SmallMArgs& a, const char** msg) {
     *msg = "small-M dgrad needs a workspace";
     return -1;
   }
-  const size_t smem = static_cast<size_t>(16) * (rps + 8) * 2 + (kWarps + 1) * kNT * 16 * 8 * 4;
+  // tensor maps: packed W [N][K(/2)], scales [N][K/32 or K/16], grad_out [M][N]
+  CUtensorMap tm_w, tm_s, tm_g;
+  const uint64_t wrow = a.fmt == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
+  {
+    const uint64_t dims[2] = {wrow, static_cast<uint64_t>(a.N)};
+    const uint64_t strides[1] = {wrow};
+    const uint32_t box[2] = {static_cast<uint32_t>(a.fmt == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2),
+                             static_cast<uint32_t>(kBox)};
+    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      *msg = "tensor map encoding failed for W";
+      return -1;
+    }
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {64, 16};
+    if (!encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
+      *msg = "tensor map encoding failed for grad_out";
+      return -1;
+    }
+  }
+  tm_s = tm_w;
+  p.scale_tma = 0;
+  if (a.fmt == BSQ_MXFP4 || a.fmt == BSQ_NVFP4) {
+    const uint64_t srow = a.fmt == BSQ_MXFP4 ? a.K / 32 : a.K / 16;
+    if (srow % 16 == 0 && (reinterpret_cast<uintptr_t>(a.w_scale) & 15u) == 0) {
+      const uint64_t dims[2] = {srow, static_cast<uint64_t>(a.N)};
+      const uint64_t strides[1] = {srow};
+      const uint32_t box[2] = {16, static_cast<uint32_t>(kBox)};
+      if (!encode_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_scale, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        *msg = "tensor map encoding failed for the scales";
+        return -1;
+      }
+      p.scale_tma = 1;
+    }
+  }
   const dim3 grid(slabs, splits);
   cudaError_t e = cudaSuccess;
+#define BSQ_LAUNCH_SMALL(F_)                                                                                 \
+  e = cudaFuncSetAttribute(smallm_dgrad_kernel<F_>, cudaFuncAttributeMaxDynamicSharedMemorySize,            \
+                           SmallFmt<F_>::kSmem);                                                             \
+  if (e == cudaSuccess) smallm_dgrad_kernel<F_><<<grid, kThreadsSm, SmallFmt<F_>::kSmem, a.stream>>>(tm_w, tm_s, tm_g, p);
   switch (a.fmt) {
-    case BSQ_MXFP4:
-      e = cudaFuncSetAttribute(smallm_dgrad_kernel<BSQ_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-      if (e == cudaSuccess) smallm_dgrad_kernel<BSQ_MXFP4><<<grid, kThreadsSm, smem, a.stream>>>(p);
-      break;
-    case BSQ_NVFP4:
-      e = cudaFuncSetAttribute(smallm_dgrad_kernel<BSQ_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-      if (e == cudaSuccess) smallm_dgrad_kernel<BSQ_NVFP4><<<grid, kThreadsSm, smem, a.stream>>>(p);
-      break;
-    case BSQ_FP8_E4M3_B128:
-      e = cudaFuncSetAttribute(smallm_dgrad_kernel<BSQ_FP8_E4M3_B128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-      if (e == cudaSuccess) smallm_dgrad_kernel<BSQ_FP8_E4M3_B128><<<grid, kThreadsSm, smem, a.stream>>>(p);
-      break;
+    case BSQ_MXFP4: BSQ_LAUNCH_SMALL(BSQ_MXFP4) break;
+    case BSQ_NVFP4: BSQ_LAUNCH_SMALL(BSQ_NVFP4) break;
+    case BSQ_FP8_E4M3_B128: BSQ_LAUNCH_SMALL(BSQ_FP8_E4M3_B128) break;
     default:
       *msg = "small-M dgrad: unsupported format";
       return -1;
   }
+#undef BSQ_LAUNCH_SMALL
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);
@@ -424,7 +481,11 @@ extern "C" bsq_status bsq_linear_dgrad_smallm_noalloc(const void* grad_out, int6
   // call uses so that an earlier interrupted call cannot leak into this one.
   e = cudaMemsetAsync(scratch, 0, bsq::smallm_workspace_bytes(K), s);
   if (e != cudaSuccess) return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, cudaGetErrorString(e)));
-  bsq::SmallMArgs a{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, M, N, K, grad_x, scratch, sms, s};
+  int32_t* errw = nullptr;
+  int sms2 = 0;
+  const int st2 = bsq::device_error_word(&errw, &sms2);
+  if (st2 != BSQ_OK) return static_cast<bsq_status>(st2);
+  bsq::SmallMArgs a{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, M, N, K, grad_x, scratch, sms, s, errw};
   const char* msg = "";
   if (bsq::launch_smallm(a, &msg) != 0) return static_cast<bsq_status>(bsq::set_error(BSQ_ERR_CUDA, msg));
   return BSQ_OK;
