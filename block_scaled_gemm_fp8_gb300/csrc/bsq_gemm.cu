@@ -13,11 +13,19 @@
 // "MN-major" A operand: no transpose kernel is needed on either side, and the
 // dequantization work per tensor-core FLOP is that of a 128-row operand.
 //
-// One persistent CTA per SM, 24 warps:
-//   warp 0      TMA producer of the packed ring: packed tile (+ FP4 scale tile) per k-block
-//   warp 3      TMA producer of the grad_out ring: up to four 64x64 BF16 boxes per k-block
-//   warp 1      MMA issuer (one thread): tcgen05.mma 128 x N x 16, FP32 accumulators in TMEM
-//   warp 2      TMEM allocation / release
+// The tensor-core work runs on CTA pairs (clusters of two SMs) with the 2-SM MMA
+// (tcgen05.mma.cta_group::2): one pair tile is 256 m x 256 n.  Each CTA dequantizes its
+// own 128 m-rows and stages half of the grad_out tile (n rows [r*Nm/2, (r+1)*Nm/2) for
+// CTA r and an MMA of width Nm); the MMA reads A and B out of both CTAs' shared memory
+// and leaves each CTA's 128 x 256 FP32 accumulator in its own TMEM.  Halving the grad_out
+// bytes each SM stages halves the L2->SM traffic per FLOP and the shared memory needed to
+// keep the TMA round trip (over a microsecond) covered.
+//
+// Per CTA (one per SM), 24 warps:
+//   warps 0, 2  TMA producers of the packed ring (alternate k-blocks): packed tile and
+//               the FP4 scale tile; warp 2 also allocates / frees TMEM
+//   warp 3      TMA producer of the grad_out ring: this CTA's half of the k-block's tile
+//   warp 1      MMA issuer, one thread of the even CTA: 4 x (256 x Nm x 16) per k-block
 //   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
 //   warps 8-23  dequantization, two teams of 8 warps taking alternate k-blocks:
 //               packed codes (smem) -> BF16, written in the 128-byte swizzled MN-major
@@ -25,12 +33,15 @@
 //               outside the current expert (wgrad)
 // Three rings decouple the chains: the packed ring (deep, small stages) feeds the
 // dequant teams; the BF16 operand ring feeds the MMA from the dequant teams; the
-// grad_out ring feeds the MMA straight from TMA.  Each buffer is held only for its own
-// chain, so TMA latency, decode time and MMA time overlap.  Two TMEM accumulators
-// (2 x 256 columns) let the epilogue of one tile overlap the main loop of the next.
-// Tiles are walked in a static persistent order; the expert of a tile comes from a
-// per-CTA prefix sum of tile counts over the offsets.  Every wait is bounded by
-// %globaltimer and records a timeout in the device error word instead of hanging.
+// grad_out ring feeds the MMA straight from TMA.  The even CTA's MMA thread waits on
+// its own barriers only: its grad_out half by TMA bytes, and "operand ready" arrivals
+// that both CTAs' dequant warps send once their A rows are written and their grad_out
+// half has landed.  MMA completion is multicast to both CTAs' "slot free" barriers.
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap the main
+// loop of the next.  Tiles are walked in a static persistent order; the expert of a
+// tile comes from a per-CTA prefix sum of tile counts over the offsets.  Every wait is
+// bounded by %globaltimer and records a timeout in the device error word (and stops the
+// peer CTA) instead of hanging.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -47,10 +58,13 @@ constexpr int kDeqTeams = 2;                    // dequant teams alternate k-blo
 constexpr int kThreads = 256 + kDeqTeams * 256;  // 8 control/epilogue warps + 8 warps per team
 constexpr int kBoxBytes = 64 * 64 * 2;          // one 64x64 BF16 box = one swizzle column of 64 rows
 constexpr int kABytes = kTileM * kTileK * 2;     // 16 KB: dequantized operand, 2 swizzle columns
-constexpr int kBBytes = kTileN * kTileK * 2;     // 32 KB: grad_out side, 4 boxes
+constexpr int kPair = 2;                         // CTAs of one 2-SM MMA (a cluster)
+constexpr uint16_t kPairMask = 3;                // both CTAs of the pair
+constexpr int kBHalf = kTileN / kPair;           // grad_out rows (n) staged by each CTA
+constexpr int kBBytes = kBHalf * kTileK * 2;     // 16 KB: this CTA's half of the grad_out tile
 constexpr int kTmemCols = 512;                   // 2 accumulators x 256 FP32 columns
 constexpr int kAStages = 3;
-constexpr int kBStages = 4;
+constexpr int kBStages = 8;
 constexpr int kMaxStages = 8;
 
 template <int FMT>
@@ -81,9 +95,12 @@ struct Params {
   int32_t N;
   int32_t Kc;
   int32_t num_m;              // ceil(Kc / 128)
+  int32_t num_mg;             // ceil(num_m / 2): m-tile pairs, one per pair tile
   int32_t scale_ld;           // scale row pitch (elements)
   int32_t scale_rblocks;      // FP8: ceil(p_rows / 128)
   int32_t scale_tma;          // FP4: scale tiles come through TMA (row pitch a multiple of 16 bytes)
+  int32_t b_mode;             // grad_out half tile per k-block: 0 = two 64x64 boxes, 1 = one 2-D box, 2 = one 3-D box
+  int32_t b_rows;             // mode 1: rows of the box (tokens); mode 2: 64-column atoms in the box
   uint64_t timeout_ns;
 };
 
@@ -107,26 +124,31 @@ struct SharedTail {
 
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 
-// Bounded wait on an mbarrier phase; false when the CTA aborted or the limit ran out.
+// Bounded wait on an mbarrier phase; false when the CTA aborted or the limit ran out.  A
+// timeout stops this CTA and its peer (both abort flags sit at the same shared offset).
+// CL: the barrier receives arrivals from the peer CTA (acquire at cluster scope).
+template <bool CL>
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              int32_t* err, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+      if (CL ? mbar_try_wait_sleep_cl(bar, parity, 20000u) : mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
+      st_rank_u32(smem_u32(const_cast<uint32_t*>(abort_flag)), cluster_ctarank() ^ 1u, 1u);
       record_error(err, BSQ_DEVERR_TIMEOUT);
       return false;
     }
   }
 }
+template <bool CL = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                            int32_t* err, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, abort_flag, err, limit_ns);
+  if (CL ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow<CL>(bar, parity, abort_flag, err, limit_ns);
 }
 
 // Ring position of the kc-th k-block: slot and the parity of the phase it fills.
@@ -144,13 +166,14 @@ struct TileInfo {
 };
 
 template <int OP>
-__device__ __forceinline__ TileInfo decode_tile(int t, int& e_cur, const SharedTail& sh, const Params& p) {
+__device__ __forceinline__ TileInfo decode_tile(int t, int& e_cur, const SharedTail& sh, const Params& p,
+                                               int rank) {
   while (sh.pre[e_cur + 1] <= t) ++e_cur;
   TileInfo ti;
   const int local = t - sh.pre[e_cur];
   ti.e = e_cur;
-  ti.mt = local % p.num_m;
-  ti.nt = local / p.num_m;
+  ti.mt = (local % p.num_mg) * kPair + rank;   // may be past the last m-tile (odd CTA of the last pair)
+  ti.nt = local / p.num_mg;
   ti.r0 = sh.off[e_cur];
   ti.r1 = sh.off[e_cur + 1];
   const int cnt = ti.r1 - ti.r0;
@@ -162,6 +185,15 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int& e_cur, const SharedT
     ti.kblocks = (cnt + kTileK - 1) / kTileK;
   }
   return ti;
+}
+
+// Width of the pair MMA for a tile with n_valid columns.  CTA r stages grad_out n rows
+// [r*Nm/2, (r+1)*Nm/2); the 3-D grad_out box (wgrad, b_mode 2) needs Nm/2 to be a whole
+// number of 64-column swizzle atoms.
+template <int OP>
+__device__ __forceinline__ int mma_width(int n_valid, int b_mode) {
+  if (OP == kWgrad && b_mode == 2) return n_valid > 128 ? 256 : 128;
+  return max(32, (n_valid + 15) & ~15);
 }
 
 template <int FMT>
@@ -207,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sh.p_empty[s]), 8);
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(smem_u32(&sh.a_full[s]), 8);
+      mbar_init(smem_u32(&sh.a_full[s]), 8 * kPair);   // one dequant team of each CTA (even CTA's is used)
       mbar_init(smem_u32(&sh.a_empty[s]), 1);
     }
     for (int s = 0; s < kBStages; ++s) {
@@ -216,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sh.tmem_full[b]), 1);
-      mbar_init(smem_u32(&sh.tmem_empty[b]), 4);
+      mbar_init(smem_u32(&sh.tmem_empty[b]), 4 * kPair);   // epilogue warps of both CTAs
     }
     mbar_init(smem_u32(&sh.drain), 1);
     sh.abort_flag = 0u;
@@ -228,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (F::kFp4 && p.scale_tma) tma_prefetch_map(&tm_s);
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&sh.tmem_base), kTmemCols);
+    tmem_relinquish_pair();
   }
   // Expert table: off[e] = start row of expert e.  A null offsets pointer is one group.
   const int E = p.E;
@@ -250,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b < a || b > p.S || a < 0) bad = 1;
       const int cnt = max(b - a, 0);
       const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
-      sum += ntiles * p.num_m;
+      sum += ntiles * p.num_mg;
     }
     int incl = sum;
 #pragma unroll
@@ -264,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sh.pre[e] = run;
       const int cnt = max(sh.off[e + 1] - sh.off[e], 0);
       const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
-      run += ntiles * p.num_m;
+      run += ntiles * p.num_mg;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
@@ -276,23 +308,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_sync();   // both CTAs of the pair have initialised their barriers before any remote arrival
   const uint32_t tmem_base = sh.tmem_base;
   const int total_tiles = sh.total_tiles;
   const uint64_t limit = p.timeout_ns;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cl_id = blockIdx.x / kPair, n_cl = gridDim.x / kPair;
 
   // ---------------------------------------------------------------- roles
-  if (warp == 0) {
-    // ===== TMA producer: packed ring =====
+  if (warp == 0 || warp == 2) {
+    // ===== TMA producers: packed ring, one warp per k-block parity =====
+    const uint32_t par = warp == 0 ? 0u : 1u;
     if (lane == 0) {
       uint32_t kc = 0;
       int e_cur = 0;
       uint32_t pend_mask = 0, pend_par = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
         const int m0 = ti.mt * kTileM;
         const int pbatch = OP == kDgrad ? ti.e : 0;
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
+          if ((kc & 1u) != par) continue;
           const Slot sl = ring_slot<kPStages>(kc);
           if (!wait_phase(smem_u32(&sh.p_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
           const uint32_t full = smem_u32(&sh.p_full[sl.idx]);
@@ -318,28 +355,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) drain_pending<kPStages>(sh.p_full, pend_mask, pend_par, limit);
     }
   } else if (warp == 3) {
-    // ===== TMA producer: grad_out ring =====
+    // ===== TMA producer: this CTA's half of the grad_out ring =====
     if (lane == 0) {
       uint32_t kc = 0;
       int e_cur = 0;
       uint32_t pend_mask = 0, pend_par = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
-        const int nbox = (ti.n_valid + 63) >> 6;
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
+        const int half = rank * (mma_width<OP>(ti.n_valid, p.b_mode) / 2);   // first n of this CTA's half
         bool ok = true;
         for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
           const Slot sl = ring_slot<kBStages>(kc);
           if (!wait_phase(smem_u32(&sh.b_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
           const uint32_t full = smem_u32(&sh.b_full[sl.idx]);
-          mbar_arrive_expect_tx(full, nbox * kBoxBytes);
           pend_mask |= 1u << sl.idx;
           pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
-          uint8_t* dst = ring_b + sl.idx * kBBytes;
-          for (int j = 0; j < nbox; ++j) {
-            if (OP == kDgrad)
-              tma_load_2d(smem_u32(dst + j * kBoxBytes), &tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + 64 * j);
-            else
-              tma_load_2d(smem_u32(dst + j * kBoxBytes), &tm_g, full, ti.nt * kTileN + 64 * j, ti.r0 + kb * kTileK);
+          const uint32_t dst = smem_u32(ring_b + sl.idx * kBBytes);
+          if (p.b_mode == 1) {
+            // dgrad: b_rows tokens x 64 columns, K-major rows of 128 bytes
+            mbar_arrive_expect_tx(full, p.b_rows * 128);
+            tma_load_2d(dst, &tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + half);
+          } else if (p.b_mode == 2) {
+            // wgrad: b_rows swizzle atoms x 64 tokens x 64 columns
+            mbar_arrive_expect_tx(full, p.b_rows * kBoxBytes);
+            tma_load_3d(dst, &tm_g, full, 0, ti.r0 + kb * kTileK, (ti.nt * kTileN + half) / 64);
+          } else {
+            // wgrad, N not a multiple of 64: two 64 x 64 boxes (the second may lie past N)
+            mbar_arrive_expect_tx(full, 2 * kBoxBytes);
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(dst + j * kBoxBytes, &tm_g, full, ti.nt * kTileN + half + 64 * j, ti.r0 + kb * kTileK);
           }
         }
         if (!ok) break;
@@ -347,49 +391,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) drain_pending<kBStages>(sh.b_full, pend_mask, pend_par, limit);
     }
   } else if (warp == 1) {
-    // ===== MMA issuer =====
-    if (lane == 0) {
-      uint32_t kc = 0;
+    // ===== MMA issuer: one thread of the even CTA drives the pair =====
+    // This thread shares its scheduler with busy dequant warps, so its per-k-block path is
+    // kept short: ring positions advance incrementally and the shared-memory descriptors
+    // are formed by adding to the 14-bit start-address field (addresses < 256 KB).
+    if (lane == 0 && rank == 0) {
+      uint32_t ia = 0, pa = 0, ib = 0, pb = 0;   // ring slot and phase parity of the next k-block
       int e_cur = 0;
       uint32_t acc = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+      const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), kBoxBytes, 1024);   // A: MN-major, atoms of 64 m at 8 KB
+      const uint64_t bdesc0 = OP == kDgrad ? sdesc_sw128(smem_u32(ring_b), 16, 1024)          // B: K-major rows
+                                           : sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B: MN-major
+      constexpr uint32_t kAStep = 2048 >> 4;                          // 16 k-rows of an MN-major tile
+      constexpr uint32_t kBStep = OP == kDgrad ? (32 >> 4) : (2048 >> 4);   // 16 k of the B tile
+      const uint32_t a_full0 = smem_u32(&sh.a_full[0]), a_empty0 = smem_u32(&sh.a_empty[0]);
+      const uint32_t b_full0 = smem_u32(&sh.b_full[0]), b_empty0 = smem_u32(&sh.b_empty[0]);
+      auto ready = [&](uint32_t sa, uint32_t qa, uint32_t sb, uint32_t qb) {
+        return wait_phase(b_full0 + 8 * sb, qb, abort_flag, p.err, limit) &&
+               wait_phase<true>(a_full0 + 8 * sa, qa, abort_flag, p.err, limit);
+      };
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
         if (ti.kblocks == 0) continue;
         const uint32_t buf = acc & 1u;
         const uint32_t acc_phase = (acc >> 1) & 1u;
-        if (!wait_phase(smem_u32(&sh.tmem_empty[buf]), acc_phase ^ 1u, abort_flag, p.err, limit)) break;
+        if (!wait_phase<true>(smem_u32(&sh.tmem_empty[buf]), acc_phase ^ 1u, abort_flag, p.err, limit)) break;
         tc_fence_after();
-        const uint32_t n_mma = (static_cast<uint32_t>(ti.n_valid) + 15u) & ~15u;
-        const uint32_t idesc = idesc_bf16_f32(kTileM, n_mma, true, OP == kWgrad);
+        const uint32_t n_mma = static_cast<uint32_t>(mma_width<OP>(ti.n_valid, p.b_mode));
+        const uint32_t idesc = idesc_bf16_f32(kPair * kTileM, n_mma, true, OP == kWgrad);
         const uint32_t d_tmem = tmem_base + buf * kTileN;
-        bool ok = true;
-        for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
-          const Slot sa = ring_slot<kAStages>(kc);
-          const Slot sb = ring_slot<kBStages>(kc);
-          if (!wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit) ||
-              !wait_phase(smem_u32(&sh.a_full[sa.idx]), sa.par, abort_flag, p.err, limit)) {
-            ok = false;
-            break;
-          }
+        // The operands of the next k-block are awaited while this k-block's MMAs are still
+        // queued, before its commits: a commit takes a slot of the short tensor instruction
+        // queue, and waiting after it would leave the tensor pipe idle.
+        bool ok = ready(ia, pa, ib, pb);
+        for (int kb = 0; ok && kb < ti.kblocks; ++kb) {
           tc_fence_after();
-          const uint32_t a_base = smem_u32(ring_a + sa.idx * kABytes);
-          const uint32_t b_base = smem_u32(ring_b + sb.idx * kBBytes);
+          const uint64_t ad = adesc0 + ia * (kABytes >> 4);
+          const uint64_t bd = bdesc0 + ib * (kBBytes >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            // A: MN-major, swizzle columns of 64 m at 8 KB, 8-row groups at 1 KB; 16 k-rows = 2 KB.
-            const uint64_t adesc = sdesc_sw128(a_base + kk * 2048, kBoxBytes, 1024);
-            uint64_t bdesc;
-            if (OP == kDgrad)  // B: K-major rows of 128 bytes (64 k), 8-row groups at 1 KB; 16 k = 32 B
-              bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
-            else               // B: MN-major like A
-              bdesc = sdesc_sw128(b_base + kk * 2048, kBoxBytes, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          umma_commit(smem_u32(&sh.a_empty[sa.idx]));
-          umma_commit(smem_u32(&sh.b_empty[sb.idx]));
+          for (int kk = 0; kk < kTileK / 16; ++kk)
+            umma_bf16_pair(d_tmem, ad + kk * kAStep, bd + kk * kBStep, idesc, (kb | kk) != 0 ? 1u : 0u);
+          const uint32_t ia_n = ia + 1 == kAStages ? 0u : ia + 1, pa_n = ia + 1 == kAStages ? pa ^ 1u : pa;
+          const uint32_t ib_n = ib + 1 == kBStages ? 0u : ib + 1, pb_n = ib + 1 == kBStages ? pb ^ 1u : pb;
+          if (kb + 1 < ti.kblocks) ok = ready(ia_n, pa_n, ib_n, pb_n);
+          umma_commit_pair(a_empty0 + 8 * ia, kPairMask);   // both CTAs may refill their slots
+          umma_commit_pair(b_empty0 + 8 * ib, kPairMask);
+          ia = ia_n; pa = pa_n; ib = ib_n; pb = pb_n;
         }
         if (!ok) break;
-        umma_commit(smem_u32(&sh.tmem_full[buf]));
+        umma_commit_pair(smem_u32(&sh.tmem_full[buf]), kPairMask);
         ++acc;
       }
     }
@@ -400,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mcol = lane_to_col<FMT>(i);
     int e_cur = 0;
     uint32_t acc = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+    for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
       const int m = ti.mt * kTileM + mcol;
       const bool mok = m < p.Kc;
       __nv_bfloat16* obase;
@@ -431,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c == nchunks - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sh.tmem_empty[buf]));
+          if (lane == 0) mbar_arrive_rank(smem_u32(&sh.tmem_empty[buf]), 0);   // the even CTA's MMA reuses it
         }
         if (mok) {
           const int nlim = min(32, ti.n_valid - c * 32);
@@ -461,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_off = F::kFp4 ? r * F::kPRowBytes + 16 * g : r * F::kPRowBytes + 32 * g + 16 * (r & 1);
     uint32_t kc = 0;                                           // k-blocks seen so far (all teams)
     int e_cur = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p);
+    for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
       const int m0 = ti.mt * kTileM;
       const int col0 = m0 + 32 * g;
       const bool col_ok = col0 < p.Kc;
@@ -578,17 +628,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ast = a_ring + sa.idx * kABytes;
 #pragma unroll
         for (int j = 0; j < 4; ++j) sts128(ast + st_off[j], v[j][0], v[j][1], v[j][2], v[j][3]);
+        // This CTA's grad_out half must have landed before the operand-ready arrival: the
+        // even CTA's MMA thread only watches its own half's bytes.
+        const Slot sb = ring_slot<kBStages>(kc);
+        ok = wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
         if (OP == kWgrad && kvalid < kTileK) {
           // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must not
-          // reach the products: zero them in every loaded box, once the boxes have landed.
-          const Slot sb = ring_slot<kBStages>(kc);
-          ok = wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
+          // reach the products: zero them in both boxes of this CTA's half.
           const uint32_t b_tile = smem_u32(ring_b + sb.idx * kBBytes);
-          const int nbox = (ti.n_valid + 63) >> 6;
           const int dt = dw * 32 + lane;
-          for (int idx = dt; idx < (kTileK - kvalid) * 8 * nbox; idx += 256) {
+          for (int idx = dt; idx < (kTileK - kvalid) * 8 * 2; idx += 256) {
             const int box = idx / ((kTileK - kvalid) * 8);
             const int rem = idx % ((kTileK - kvalid) * 8);
             const int rr = kvalid + rem / 8, c = rem % 8;
@@ -597,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.a_full[sa.idx]));
+        if (lane == 0) mbar_arrive_rank(smem_u32(&sh.a_full[sa.idx]), 0);
       }
       if (!ok) break;
     }
@@ -605,9 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
-  if (warp == 1 && lane == 0) {
-    // Every MMA this thread issued has completed once the drain barrier fires.
-    umma_commit(smem_u32(&sh.drain));
+  if (warp == 1 && lane == 0 && rank == 0) {
+    // Every MMA this thread issued has completed (and read the odd CTA's shared memory)
+    // once the drain barrier fires.
+    umma_commit_pair(smem_u32(&sh.drain), 1);
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(smem_u32(&sh.drain), 0) && global_timer_ns() - t0 < limit) {
     }
@@ -615,7 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+  // No CTA leaves while its peer may still arrive on its barriers or read its operands.
+  cluster_sync();
+  if (warp == 2) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -652,12 +706,32 @@ template <int FMT, int OP>
 int launch_typed(const GemmArgs& a, const char** msg) {
   using F = Fmt<FMT>;
   CUtensorMap tm_p, tm_g;
+  int b_mode = 0, b_rows = 0;
   {
+    // this CTA's half of a k-block's grad_out tile in a single TMA copy where the shape allows it
     const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.S)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
-    const uint32_t box[2] = {64, 64};
-    if (!encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B)) {
+    bool ok = false;
+    if (OP == kDgrad) {
+      b_rows = static_cast<int>(a.S < kBHalf ? a.S : kBHalf);
+      const uint32_t box[2] = {64, static_cast<uint32_t>(b_rows)};
+      ok = encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      b_mode = 1;
+    } else if (a.N % 64 == 0) {
+      // [N/64 swizzle columns][S tokens][64 columns] view of grad_out
+      b_rows = static_cast<int>(a.N / 64 < kBHalf / 64 ? a.N / 64 : kBHalf / 64);
+      const uint64_t d3[3] = {64, static_cast<uint64_t>(a.S), static_cast<uint64_t>(a.N / 64)};
+      const uint64_t s3[2] = {static_cast<uint64_t>(a.N) * 2, 128};
+      const uint32_t box[3] = {64, 64, static_cast<uint32_t>(b_rows)};
+      ok = encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.g, d3, s3, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      b_mode = 2;
+    }
+    if (!ok && OP != kDgrad) {
+      const uint32_t box[2] = {64, 64};
+      ok = encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      b_mode = 0;
+    }
+    if (!ok) {
       *msg = "tensor map encoding failed for grad_out";
       return -1;
     }
@@ -702,6 +776,8 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   }
   Params p;
   p.scale_tma = scale_tma;
+  p.b_mode = b_mode;
+  p.b_rows = b_rows;
   p.scale = static_cast<const uint8_t*>(a.p_scale);
   p.tensor_scale = a.p_tensor_scale;
   p.offsets = a.offsets;
@@ -714,24 +790,45 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   p.N = static_cast<int32_t>(a.N);
   p.Kc = static_cast<int32_t>(a.kc);
   p.num_m = static_cast<int32_t>((a.kc + kTileM - 1) / kTileM);
+  p.num_mg = (p.num_m + kPair - 1) / kPair;
   p.scale_ld = FMT == BSQ_MXFP4 ? static_cast<int32_t>(a.kc / 32)
                : FMT == BSQ_NVFP4 ? static_cast<int32_t>(a.kc / 16)
                                   : static_cast<int32_t>((a.kc + 127) / 128);
   p.scale_rblocks = static_cast<int32_t>((a.p_rows + 127) / 128);
   p.timeout_ns = wait_limit_ns();
 
-  // Upper bound of the tile count (the exact count depends on the offsets, read on the device).
+  // Upper bound of the pair-tile count (the exact count depends on the offsets, read on the device).
   const int64_t nn = (a.N + kTileN - 1) / kTileN;
-  const int64_t bound = OP == kDgrad ? p.num_m * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_m * nn * a.E;
-  int64_t grid = bound < a.num_sms ? bound : a.num_sms;
-  if (grid < 1) grid = 1;
+  const int64_t bound = OP == kDgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
   auto kern = bsq_gemm_kernel<FMT, OP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e == cudaSuccess) {
-    kern<<<dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, a.stream>>>(tm_p, tm_g, tm_s, p);
-    e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent grid: as many pairs as can be resident at once (a GPC with an odd number of
+  // free SMs leaves one idle), never more than there are pair tiles.
+  static int max_clusters = 0;
+  if (e == cudaSuccess && max_clusters == 0) {
+    cfg.gridDim = dim3(kPair * (a.num_sms / kPair));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    max_clusters = n > 0 ? n : a.num_sms / kPair;
   }
+  int64_t clusters = bound < max_clusters ? bound : max_clusters;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kPair));
+  if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, tm_p, tm_g, tm_s, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);
     return static_cast<int>(e);
