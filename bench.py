@@ -19,7 +19,9 @@ step); value = all ranks' FLOPs / the slowest rank's time.
 """
 
 import argparse
+import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -93,6 +95,34 @@ def peaks():
         if hbm and bf16:
             return {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# The GEMM kernel's sources: a traffic figure captured from an earlier build is reported
+# only while these are unchanged.
+KERNEL_SOURCES = ["bsq_gemm.cu", "bsq_decode.cuh", "bsq_ptx.cuh", "bsq_internal.h"]
+
+
+def kernel_source_sha1():
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_scaled_gemm_fp8_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload, op):
+    """DRAM bytes (read + write) per launch of the GEMM kernel for `op` on `workload`, from
+    the committed ncu summary profiles/bsq_gemm_kernel_<workload>.md (its `traffic:` lines),
+    or None when there is no such capture or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"bsq_gemm_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha1()
+    for line in open(path):
+        m = re.match(r"\s*traffic:\s*op=(\w+)\s+bytes=(\d+)\s+source_sha1=([0-9a-f]+)", line)
+        if m and m.group(1) == op and m.group(3) == sha:
+            return int(m.group(2))
+    return None
 
 
 class ClockSampler:
@@ -408,7 +438,7 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": dom_bytes / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(c["name"], dom)
     roof["kernel"] = f"bsq_gemm_kernel ({dom})"
     roof["peak_source"] = pk["source"]
 
