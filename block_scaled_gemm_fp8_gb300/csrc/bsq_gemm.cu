@@ -63,8 +63,9 @@ constexpr uint16_t kPairMask = 3;                // both CTAs of the pair
 constexpr int kBHalf = kTileN / kPair;           // grad_out rows (n) staged by each CTA
 constexpr int kBBytes = kBHalf * kTileK * 2;     // 16 KB: this CTA's half of the grad_out tile
 constexpr int kTmemCols = 512;                   // 2 accumulators x 256 FP32 columns
-constexpr int kAStages = 3;
-constexpr int kBStages = 8;
+constexpr int kAStages = 5;
+constexpr int kBStages = 6;
+static_assert(kAStages >= 4 && kBStages >= 4, "the MMA issuer awaits two k-blocks ahead of its commits");
 constexpr int kMaxStages = 8;
 
 template <int FMT>
@@ -405,10 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kAStep = 2048 >> 4;                          // 16 k-rows of an MN-major tile
       constexpr uint32_t kBStep = OP == kDgrad ? (32 >> 4) : (2048 >> 4);   // 16 k of the B tile
       const uint32_t a_full0 = smem_u32(&sh.a_full[0]), a_empty0 = smem_u32(&sh.a_empty[0]);
-      const uint32_t b_full0 = smem_u32(&sh.b_full[0]), b_empty0 = smem_u32(&sh.b_empty[0]);
-      auto ready = [&](uint32_t sa, uint32_t qa, uint32_t sb, uint32_t qb) {
-        return wait_phase(b_full0 + 8 * sb, qb, abort_flag, p.err, limit) &&
-               wait_phase<true>(a_full0 + 8 * sa, qa, abort_flag, p.err, limit);
+      const uint32_t b_empty0 = smem_u32(&sh.b_empty[0]);
+      // A k-block is ready once both CTAs' operand-ready arrivals are in: each dequant warp
+      // arrives only after it has seen its own CTA's grad_out half land, so the grad_out
+      // halves need no wait of their own here.
+      auto ready = [&](uint32_t sa, uint32_t qa) {
+        return wait_phase<true>(a_full0 + 8 * sa, qa, abort_flag, p.err, limit);
       };
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
         const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
@@ -420,23 +423,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t n_mma = static_cast<uint32_t>(mma_width<OP>(ti.n_valid, p.b_mode));
         const uint32_t idesc = idesc_bf16_f32(kPair * kTileM, n_mma, true, OP == kWgrad);
         const uint32_t d_tmem = tmem_base + buf * kTileN;
-        // The operands of the next k-block are awaited while this k-block's MMAs are still
-        // queued, before its commits: a commit takes a slot of the short tensor instruction
-        // queue, and waiting after it would leave the tensor pipe idle.
-        bool ok = ready(ia, pa, ib, pb);
-        for (int kb = 0; ok && kb < ti.kblocks; ++kb) {
+        // k-blocks go in rounds of two: eight MMAs, then the next round's operands are
+        // awaited while those MMAs are still queued, then the round's commits (a commit
+        // takes a slot of the tensor instruction queue; waiting after it would leave the
+        // pipe idle).  The next round's operand slots were released two rounds earlier,
+        // which needs at least four operand stages.
+        auto adv = [](uint32_t& i, uint32_t& ph, uint32_t n) {
+          if (++i == n) {
+            i = 0;
+            ph ^= 1u;
+          }
+        };
+        bool ok = ready(ia, pa);
+        if (ok && ti.kblocks > 1) {
+          uint32_t xa = ia, xpa = pa;
+          adv(xa, xpa, kAStages);
+          ok = ready(xa, xpa);
+        }
+        for (int kb = 0; ok && kb < ti.kblocks; kb += 2) {
+          const int nk = kb + 1 < ti.kblocks ? 2 : 1;
           tc_fence_after();
-          const uint64_t ad = adesc0 + ia * (kABytes >> 4);
-          const uint64_t bd = bdesc0 + ib * (kBBytes >> 4);
+          uint32_t sa[2], sb[2];
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk)
-            umma_bf16_pair(d_tmem, ad + kk * kAStep, bd + kk * kBStep, idesc, (kb | kk) != 0 ? 1u : 0u);
-          const uint32_t ia_n = ia + 1 == kAStages ? 0u : ia + 1, pa_n = ia + 1 == kAStages ? pa ^ 1u : pa;
-          const uint32_t ib_n = ib + 1 == kBStages ? 0u : ib + 1, pb_n = ib + 1 == kBStages ? pb ^ 1u : pb;
-          if (kb + 1 < ti.kblocks) ok = ready(ia_n, pa_n, ib_n, pb_n);
-          umma_commit_pair(a_empty0 + 8 * ia, kPairMask);   // both CTAs may refill their slots
-          umma_commit_pair(b_empty0 + 8 * ib, kPairMask);
-          ia = ia_n; pa = pa_n; ib = ib_n; pb = pb_n;
+          for (int h = 0; h < 2; ++h) {
+            if (h < nk) {
+              const uint64_t ad = adesc0 + ia * (kABytes >> 4);
+              const uint64_t bd = bdesc0 + ib * (kBBytes >> 4);
+#pragma unroll
+              for (int kk = 0; kk < kTileK / 16; ++kk)
+                umma_bf16_pair(d_tmem, ad + kk * kAStep, bd + kk * kBStep, idesc, ((kb + h) | kk) != 0 ? 1u : 0u);
+              sa[h] = ia; sb[h] = ib;
+              adv(ia, pa, kAStages); adv(ib, pb, kBStages);
+            }
+          }
+          if (kb + 2 < ti.kblocks) {
+            ok = ready(ia, pa);
+            if (ok && kb + 3 < ti.kblocks) {
+              uint32_t xa = ia, xpa = pa;
+              adv(xa, xpa, kAStages);
+              ok = ready(xa, xpa);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h < nk) {
+              umma_commit_pair(a_empty0 + 8 * sa[h], kPairMask);
+              umma_commit_pair(b_empty0 + 8 * sb[h], kPairMask);
+            }
+          }
         }
         if (!ok) break;
         umma_commit_pair(smem_u32(&sh.tmem_full[buf]), kPairMask);

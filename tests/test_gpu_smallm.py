@@ -1,7 +1,9 @@
 """Split-K small-M dgrad (M <= 16 token rows) against the oracle.
 
-These shapes force many row splits per column slab, ragged row ranges, a ragged last
-slab and repeated calls that reuse (and must leave zeroed) the FP32 workspace."""
+These shapes cover clusters of 1, 2, 4 and 8 row splits (reduced in distributed shared
+memory), several clusters per column slab (reduced through the FP32 workspace), ragged
+row ranges, a ragged last slab and repeated calls that reuse (and must leave zeroed)
+the workspace."""
 
 import numpy as np
 import pytest
@@ -18,7 +20,7 @@ FMTS = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4]
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 384), (1, 4096, 4096), (7, 304, 4096), (16, 2000, 96 * 2),
-                                   (3, 16, 64), (16, 8, 4096)])
+                                   (3, 16, 64), (16, 8, 4096), (16, 128, 4096), (5, 8192, 1024)])
 def test_small_m_dgrad(fmt, M, N, K):
     if fmt != synth.FMT_FP8 and K % 32:
         pytest.skip("FP4 needs K % 32")
