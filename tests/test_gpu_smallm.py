@@ -1,9 +1,8 @@
 """Split-K small-M dgrad (M <= 16 token rows) against the oracle.
 
-These shapes cover clusters of 1, 2, 4 and 8 row splits (reduced in distributed shared
-memory), several clusters per column slab (reduced through the FP32 workspace), ragged
-row ranges, a ragged last slab and repeated calls that reuse (and must leave zeroed)
-the workspace."""
+These shapes force one to many row splits per column slab (N from 8 to 8192 rows),
+ragged row ranges, a ragged last slab and repeated calls that reuse (and must leave
+zeroed) the FP32 workspace."""
 
 import numpy as np
 import pytest
