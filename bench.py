@@ -264,43 +264,90 @@ def time_small_m(c, bsq, steps, warmup, flush):
 
 
 def time_e2e(c, outs, bsq, steps, warmup):
-    """Same ops through the ABI with inputs copied from pinned host memory and results read back."""
-    dev = c["G"].device
-    host_in, dev_in = [], []
+    """Same ops through the ABI with every step's inputs copied from pinned host memory and
+    its gradients copied back, pipelined the way a training loop prefetches: three streams
+    (copy-in, compute, copy-out) and two device buffer sets, so that step i+1's inputs load
+    while step i computes and step i-1's gradients drain.  Returns (ms per step, bytes in,
+    bytes out per step)."""
+    import dataclasses
 
-    def pin(t):
+    def pinned(t):
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         h.copy_(t)
-        host_in.append(h)
-        dev_in.append(t)
+        return h
 
-    pin(c["G"])
-    for p in (c["W"], c["X"]):
-        if p is None:
-            continue
-        for t in (p.data, p.scale, p.tensor_scale):
-            if t is not None:
-                pin(t)
-    host_out = {n: torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for n, o in outs.items()}
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
-    d2h = sum(h.numel() * h.element_size() for h in host_out.values())
-    stream = torch.cuda.current_stream()
+    def like(t):
+        return None if t is None else torch.empty_like(t)
 
-    def step():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        run_ops(c, outs, bsq)
-        for n, o in outs.items():
-            host_out[n].copy_(o, non_blocking=True)
+    # the step's inputs on the host
+    host = {"G": pinned(c["G"])}
+    for name in ("W", "X"):
+        pk = c[name]
+        if pk is not None:
+            host[name] = {k: pinned(getattr(pk, k)) for k in ("data", "scale", "tensor_scale")
+                          if getattr(pk, k) is not None}
+    if c["grouped"]:
+        host["offsets"] = pinned(c["offsets_dev"])
+    slots = []
+    for _ in range(2):
+        d = {"G": like(c["G"])}
+        for name in ("W", "X"):
+            pk = c[name]
+            if pk is not None:
+                d[name] = dataclasses.replace(pk, data=like(pk.data), scale=like(pk.scale),
+                                              tensor_scale=like(pk.tensor_scale))
+        if c["grouped"]:
+            d["offsets"] = like(c["offsets_dev"])
+        d["out"] = {n: torch.empty_like(o) for n, o in outs.items()}
+        d["host_out"] = {n: torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for n, o in outs.items()}
+        slots.append(d)
+    h2d = host["G"].numel() * host["G"].element_size()
+    h2d += sum(t.numel() * t.element_size() for name in ("W", "X") if name in host for t in host[name].values())
+    if c["grouped"]:
+        h2d += host["offsets"].numel() * host["offsets"].element_size()
+    d2h = sum(o.numel() * o.element_size() for o in outs.values())
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    for _ in range(warmup):
-        step()
+    def step(i):
+        k = i % 2
+        d = slots[k]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_comp[k])       # step i-2 has finished reading this buffer set
+            d["G"].copy_(host["G"], non_blocking=True)
+            for name in ("W", "X"):
+                if name in host:
+                    for f, h in host[name].items():
+                        getattr(d[name], f).copy_(h, non_blocking=True)
+            if c["grouped"]:
+                d["offsets"].copy_(host["offsets"], non_blocking=True)
+            ev_in[k].record(s_in)
+        s_comp.wait_event(ev_in[k])
+        s_comp.wait_event(ev_out[k])          # step i-2's gradients have been read back
+        cc = dict(c)
+        cc["G"] = d["G"]
+        cc["W"] = d["W"]
+        cc["X"] = d.get("X")
+        if c["grouped"]:
+            cc["offsets_dev"] = d["offsets"]
+        run_ops(cc, d["out"], bsq, stream=s_comp)
+        ev_comp[k].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k])
+            for n, o in d["out"].items():
+                d["host_out"][n].copy_(o, non_blocking=True)
+            ev_out[k].record(s_out)
+
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(s_in)
+    for i in range(steps):
+        step(warmup + i)
+    b.record(s_out)                           # after the last step's read-back
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps, h2d, d2h
 
