@@ -22,24 +22,28 @@
 // keep the TMA round trip (over a microsecond) covered.
 //
 // Per CTA (one per SM), 24 warps:
-//   warps 0, 2  TMA producers of the packed ring (alternate k-blocks): packed tile and
-//               the FP4 scale tile; warp 2 also allocates / frees TMEM
-//   warp 3      TMA producer of the grad_out ring: this CTA's half of the k-block's tile
+//   warp 0      TMA producer of the packed ring: packed tiles and FP4 scale tiles
+//   warp 2      allocates / frees TMEM
+//   warp 3      TMA producer of the grad_out ring: this CTA's half of the unit's tiles
 //   warp 1      MMA issuer, one thread of the even CTA: 4 x (256 x Nm x 16) per k-block
 //   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
-//   warps 8-23  dequantization, two teams of 8 warps taking alternate k-blocks:
-//               packed codes (smem) -> BF16, written in the 128-byte swizzled MN-major
-//               layout the tensor core reads; also zero the rows of a k-block that lie
-//               outside the current expert (wgrad)
-// Three rings decouple the chains: the packed ring (deep, small stages) feeds the
-// dequant teams; the BF16 operand ring feeds the MMA from the dequant teams; the
-// grad_out ring feeds the MMA straight from TMA.  The even CTA's MMA thread waits on
-// its own barriers only: its grad_out half by TMA bytes, and "operand ready" arrivals
-// that both CTAs' dequant warps send once their A rows are written and their grad_out
-// half has landed.  MMA completion is multicast to both CTAs' "slot free" barriers.
-// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap the main
-// loop of the next.  Tiles are walked in a static persistent order; the expert of a
-// tile comes from a per-CTA prefix sum of tile counts over the offsets.  Every wait is
+//   warps 8-23  dequantization, two teams of 8 warps; team t takes k-block t of every
+//               unit: packed codes (smem) -> BF16, written in the 128-byte swizzled
+//               MN-major layout the tensor core reads; also zero the rows of a k-block
+//               that lie outside the current expert (wgrad)
+// Three rings decouple the chains: the packed ring feeds the dequant teams; the BF16
+// operand ring feeds the MMA from the dequant teams; the grad_out ring feeds the MMA
+// straight from TMA.  All three move in units of two k-blocks, and every barrier phase
+// of a ring is waited on by the same threads in unit order (a parity wait cannot then
+// mistake a phase two laps away for its own).  The operand and grad_out rings share
+// their "slot free" barrier, so the single MMA thread handles one wait, eight MMAs and
+// one commit per unit.  It waits on its own CTA's "operand ready" barrier only, which
+// every dequant warp of both CTAs arrives on once its A rows are written and its own
+// CTA's grad_out half has landed.  MMA completion is multicast to both CTAs' "slot
+// free" barriers.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
+// overlap the main loop of the next.  Tiles are walked in a static persistent order;
+// each role finds a tile's expert with its own forward cursor over the offsets (read
+// through the read-only cache, so no table takes shared memory).  Every wait is
 // bounded by %globaltimer and records a timeout in the device error word (and stops the
 // peer CTA) instead of hanging.
 #include <cuda_bf16.h>
@@ -63,9 +67,14 @@ constexpr uint16_t kPairMask = 3;                // both CTAs of the pair
 constexpr int kBHalf = kTileN / kPair;           // grad_out rows (n) staged by each CTA
 constexpr int kBBytes = kBHalf * kTileK * 2;     // 16 KB: this CTA's half of the grad_out tile
 constexpr int kTmemCols = 512;                   // 2 accumulators x 256 FP32 columns
-constexpr int kAStages = 5;
-constexpr int kBStages = 6;
-static_assert(kAStages >= 4 && kBStages >= 4, "the MMA issuer awaits two k-blocks ahead of its commits");
+// The operand and grad_out rings move in units of two k-blocks: one "operand ready"
+// barrier, one MMA-completion commit and one grad_out barrier per unit.
+constexpr int kUnitKb = 2;
+constexpr int kAUnitBytes = kUnitKb * kABytes;   // 32 KB
+constexpr int kBUnitBytes = kUnitKb * kBBytes;   // 32 KB
+constexpr int kUStages = 3;
+static_assert(kUStages >= 2, "the MMA issuer awaits the next unit before committing the current one");
+static_assert(kDeqTeams == kUnitKb, "dequant team t fills k-block t of every unit");
 constexpr int kMaxStages = 8;
 
 template <int FMT>
@@ -78,9 +87,12 @@ struct Fmt {
   static constexpr int kPRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kTileM : kTileM / 2;
   // FP4 scale tile staged by TMA: 64 rows x 16 bytes (a 16-byte aligned window of the row's scales)
   static constexpr int kSBytes = kFp4 ? kTileK * 16 : 0;
-  static constexpr int kPStageBytes = (kPBytes + kSBytes + 1023) / 1024 * 1024;
-  static constexpr int kPStages = FMT == BSQ_BF16 ? 2 : (FMT == BSQ_FP8_E4M3_B128 ? 5 : 6);
-  static constexpr int kRingBytes = kBStages * kBBytes + kAStages * kABytes + kPStages * kPStageBytes;
+  static constexpr int kPStageBytes = (kPBytes + kSBytes + 1023) / 1024 * 1024;   // one k-block
+  static constexpr int kPUnitBytes = kUnitKb * kPStageBytes;
+  // Units of the packed ring.  Like the other rings it moves in units that both dequant
+  // teams consume in order, so no parity wait can alias a phase two laps away.
+  static constexpr int kPUnits = FMT == BSQ_BF16 ? 1 : (FMT == BSQ_FP8_E4M3_B128 ? 2 : 3);
+  static constexpr int kRingBytes = kUStages * (kBUnitBytes + kAUnitBytes) + kPUnits * kPUnitBytes;
 };
 
 struct Params {
@@ -106,12 +118,11 @@ struct Params {
 };
 
 struct SharedTail {
-  uint64_t p_full[kMaxStages];
-  uint64_t p_empty[kMaxStages];
-  uint64_t a_full[kMaxStages];
-  uint64_t a_empty[kMaxStages];
-  uint64_t b_full[kMaxStages];
-  uint64_t b_empty[kMaxStages];
+  uint64_t p_full[kMaxStages];    // per unit: the packed tiles landed (TMA bytes)
+  uint64_t p_empty[kMaxStages];   // per unit: every dequant warp of this CTA has read its half
+  uint64_t a_full[kMaxStages];    // per unit: both CTAs' dequant warps (operand written, grad_out seen)
+  uint64_t op_empty[kMaxStages];  // per unit: the unit's MMAs completed (frees its A and B slots)
+  uint64_t b_full[kMaxStages];    // per unit: this CTA's grad_out half landed (TMA bytes)
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -119,8 +130,6 @@ struct SharedTail {
   uint32_t abort_flag;
   int32_t total_tiles;
   int32_t pad;
-  int32_t off[kMaxExperts + 1];  // off[e] = first row of expert e, off[E] = end
-  int32_t pre[kMaxExperts + 1];  // prefix of tile counts
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
@@ -152,31 +161,61 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   return wait_phase_slow<CL>(bar, parity, abort_flag, err, limit_ns);
 }
 
-// Ring position of the kc-th k-block: slot and the parity of the phase it fills.
+// Ring position of the u-th unit: slot and the parity of the phase it fills.
 struct Slot {
   int idx;
   uint32_t par;
 };
 template <int N>
-__device__ __forceinline__ Slot ring_slot(uint32_t kc) {
-  return Slot{static_cast<int>(kc % N), (kc / N) & 1u};
+__device__ __forceinline__ Slot ring_slot(uint32_t u) {
+  return Slot{static_cast<int>(u % N), (u / N) & 1u};
 }
 
 struct TileInfo {
   int e, mt, nt, n_valid, kblocks, r0, r1;
 };
 
+// Pair tiles of an expert with cnt rows, and one past the last row of expert e (the
+// cumulative end offset; a null offsets pointer is one group of S rows).
 template <int OP>
-__device__ __forceinline__ TileInfo decode_tile(int t, int& e_cur, const SharedTail& sh, const Params& p,
-                                               int rank) {
-  while (sh.pre[e_cur + 1] <= t) ++e_cur;
+__device__ __forceinline__ int expert_tiles(const Params& p, int cnt) {
+  const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
+  return ntiles * p.num_mg;
+}
+__device__ __forceinline__ int expert_end(const Params& p, int e) { return p.offsets ? __ldg(p.offsets + e) : p.S; }
+
+// Each role walks the tiles in the same increasing order and keeps its own cursor over the
+// experts: tiles [pre, next) belong to expert e, whose rows are [r0, r1).
+struct ExpertCursor {
+  int e, pre, next, r0, r1;
+};
+template <int OP>
+__device__ __forceinline__ ExpertCursor cursor_begin(const Params& p) {
+  ExpertCursor c;
+  c.e = 0;
+  c.pre = 0;
+  c.r0 = 0;
+  c.r1 = expert_end(p, 0);
+  c.next = expert_tiles<OP>(p, c.r1);
+  return c;
+}
+
+template <int OP>
+__device__ __forceinline__ TileInfo decode_tile(int t, ExpertCursor& c, const Params& p, int rank) {
+  while (c.next <= t) {   // t < total tiles, so this stops at an expert below E
+    ++c.e;
+    c.pre = c.next;
+    c.r0 = c.r1;
+    c.r1 = expert_end(p, c.e);
+    c.next = c.pre + expert_tiles<OP>(p, c.r1 - c.r0);
+  }
   TileInfo ti;
-  const int local = t - sh.pre[e_cur];
-  ti.e = e_cur;
+  const int local = t - c.pre;
+  ti.e = c.e;
   ti.mt = (local % p.num_mg) * kPair + rank;   // may be past the last m-tile (odd CTA of the last pair)
   ti.nt = local / p.num_mg;
-  ti.r0 = sh.off[e_cur];
-  ti.r1 = sh.off[e_cur + 1];
+  ti.r0 = c.r0;
+  ti.r1 = c.r1;
   const int cnt = ti.r1 - ti.r0;
   if (OP == kDgrad) {
     ti.n_valid = min(kTileN, cnt - ti.nt * kTileN);
@@ -220,12 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_g,
                     const __grid_constant__ CUtensorMap tm_s, const Params p) {
   using F = Fmt<FMT>;
-  constexpr int kPStages = F::kPStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring_b = smem;
-  uint8_t* ring_a = ring_b + kBStages * kBBytes;
-  uint8_t* ring_p = ring_a + kAStages * kABytes;
+  uint8_t* ring_a = ring_b + kUStages * kBUnitBytes;
+  uint8_t* ring_p = ring_a + kUStages * kAUnitBytes;
   SharedTail& sh = *reinterpret_cast<SharedTail*>(smem + F::kRingBytes);
   volatile uint32_t* abort_flag = &sh.abort_flag;
 
@@ -235,17 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- set-up
   if (tid == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < F::kPUnits; ++s) {
       mbar_init(smem_u32(&sh.p_full[s]), 1);
-      mbar_init(smem_u32(&sh.p_empty[s]), 8);
+      mbar_init(smem_u32(&sh.p_empty[s]), 8 * kDeqTeams);   // every dequant warp of this CTA
     }
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(smem_u32(&sh.a_full[s]), 8 * kPair);   // one dequant team of each CTA (even CTA's is used)
-      mbar_init(smem_u32(&sh.a_empty[s]), 1);
-    }
-    for (int s = 0; s < kBStages; ++s) {
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(smem_u32(&sh.a_full[s]), 8 * kDeqTeams * kPair);   // every dequant warp of both CTAs (even CTA's is used)
+      mbar_init(smem_u32(&sh.op_empty[s]), 1);
       mbar_init(smem_u32(&sh.b_full[s]), 1);
-      mbar_init(smem_u32(&sh.b_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sh.tmem_full[b]), 1);
@@ -264,44 +299,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(smem_u32(&sh.tmem_base), kTmemCols);
     tmem_relinquish_pair();
   }
-  // Expert table: off[e] = start row of expert e.  A null offsets pointer is one group.
   const int E = p.E;
-  for (int e = tid; e <= E; e += kThreads) {
-    int v;
-    if (e == 0) v = 0;
-    else v = p.offsets ? __ldg(p.offsets + (e - 1)) : p.S;
-    sh.off[e] = v;
-  }
-  __syncthreads();
   if (warp == 3) {
-    // Validate and prefix-sum the tile counts: lane l owns experts [l*per, (l+1)*per).
+    // Validate the offsets and count the tiles: lane l owns experts [l*per, (l+1)*per).
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int bad = 0, sum = 0;
+    int a = e0 == 0 ? 0 : expert_end(p, e0 - 1);
     for (int e = e0; e < e1; ++e) {
-      const int a = sh.off[e], b = sh.off[e + 1];
+      const int b = expert_end(p, e);
       if (b < a || b > p.S || a < 0) bad = 1;
-      const int cnt = max(b - a, 0);
-      const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
-      sum += ntiles * p.num_mg;
-    }
-    int incl = sum;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
+      sum += expert_tiles<OP>(p, max(b - a, 0));
+      a = b;
     }
     bad = __any_sync(0xffffffffu, bad);
-    int run = incl - sum;
-    for (int e = e0; e < e1; ++e) {
-      sh.pre[e] = run;
-      const int cnt = max(sh.off[e + 1] - sh.off[e], 0);
-      const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
-      run += ntiles * p.num_mg;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(sum)));
     if (lane == 0) {
-      sh.pre[E] = total;
       sh.total_tiles = bad ? 0 : total;
       if (bad && blockIdx.x == 0) record_error(p.err, BSQ_DEVERR_BAD_OFFSETS);
     }
@@ -317,104 +330,111 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cl_id = blockIdx.x / kPair, n_cl = gridDim.x / kPair;
 
   // ---------------------------------------------------------------- roles
-  if (warp == 0 || warp == 2) {
-    // ===== TMA producers: packed ring, one warp per k-block parity =====
-    const uint32_t par = warp == 0 ? 0u : 1u;
+  if (warp == 0) {
+    // ===== TMA producer: packed ring, one unit (two k-blocks) per barrier =====
     if (lane == 0) {
-      uint32_t kc = 0;
-      int e_cur = 0;
+      uint32_t uc = 0;
+      ExpertCursor cur = cursor_begin<OP>(p);
       uint32_t pend_mask = 0, pend_par = 0;
+      const uint32_t kb_bytes = F::kPBytes + ((F::kFp4 && p.scale_tma) ? F::kSBytes : 0);
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
+        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
         const int m0 = ti.mt * kTileM;
         const int pbatch = OP == kDgrad ? ti.e : 0;
+        const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
         bool ok = true;
-        for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
-          if ((kc & 1u) != par) continue;
-          const Slot sl = ring_slot<kPStages>(kc);
+        for (int j = 0; j < units; ++j, ++uc) {
+          const Slot sl = ring_slot<F::kPUnits>(uc);
           if (!wait_phase(smem_u32(&sh.p_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
           const uint32_t full = smem_u32(&sh.p_full[sl.idx]);
-          mbar_arrive_expect_tx(full, F::kPBytes + ((F::kFp4 && p.scale_tma) ? F::kSBytes : 0));
+          const int nk = min(kUnitKb, ti.kblocks - kUnitKb * j);
+          mbar_arrive_expect_tx(full, nk * kb_bytes);
           pend_mask |= 1u << sl.idx;
           pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
-          const int prow = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
-          uint8_t* dst = ring_p + sl.idx * F::kPStageBytes;
-          if (FMT == BSQ_BF16) {
-            tma_load_3d(smem_u32(dst), &tm_p, full, m0, prow, pbatch);
-            tma_load_3d(smem_u32(dst + kBoxBytes), &tm_p, full, m0 + 64, prow, pbatch);
-          } else {
-            tma_load_3d(smem_u32(dst), &tm_p, full, FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2, prow, pbatch);
-            if (F::kFp4 && p.scale_tma) {
-              // 16-byte aligned window holding this tile's scales (4 or 8 bytes per row)
-              const int xs = (FMT == BSQ_MXFP4 ? (m0 >> 5) : (m0 >> 4)) & ~15;
-              tma_load_3d(smem_u32(dst + F::kPBytes), &tm_s, full, xs, prow, pbatch);
+          for (int h = 0; h < nk; ++h) {
+            const int kb = kUnitKb * j + h;
+            const int prow = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
+            uint8_t* dst = ring_p + sl.idx * F::kPUnitBytes + h * F::kPStageBytes;
+            if (FMT == BSQ_BF16) {
+              tma_load_3d(smem_u32(dst), &tm_p, full, m0, prow, pbatch);
+              tma_load_3d(smem_u32(dst + kBoxBytes), &tm_p, full, m0 + 64, prow, pbatch);
+            } else {
+              tma_load_3d(smem_u32(dst), &tm_p, full, FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2, prow, pbatch);
+              if (F::kFp4 && p.scale_tma) {
+                // 16-byte aligned window holding this tile's scales (4 or 8 bytes per row)
+                const int xs = (FMT == BSQ_MXFP4 ? (m0 >> 5) : (m0 >> 4)) & ~15;
+                tma_load_3d(smem_u32(dst + F::kPBytes), &tm_s, full, xs, prow, pbatch);
+              }
             }
           }
         }
         if (!ok) break;
       }
-      if (*abort_flag) drain_pending<kPStages>(sh.p_full, pend_mask, pend_par, limit);
+      if (*abort_flag) drain_pending<F::kPUnits>(sh.p_full, pend_mask, pend_par, limit);
     }
   } else if (warp == 3) {
-    // ===== TMA producer: this CTA's half of the grad_out ring =====
+    // ===== TMA producer: this CTA's half of the grad_out ring, one unit at a time =====
     if (lane == 0) {
-      uint32_t kc = 0;
-      int e_cur = 0;
+      uint32_t uc = 0;
+      ExpertCursor cur = cursor_begin<OP>(p);
       uint32_t pend_mask = 0, pend_par = 0;
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
+        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
         const int half = rank * (mma_width<OP>(ti.n_valid, p.b_mode) / 2);   // first n of this CTA's half
+        // bytes of one k-block's half tile
+        const uint32_t kb_bytes = p.b_mode == 1 ? p.b_rows * 128 : (p.b_mode == 2 ? p.b_rows : 2) * kBoxBytes;
+        const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
         bool ok = true;
-        for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
-          const Slot sl = ring_slot<kBStages>(kc);
-          if (!wait_phase(smem_u32(&sh.b_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
+        for (int j = 0; j < units; ++j, ++uc) {
+          const Slot sl = ring_slot<kUStages>(uc);
+          if (!wait_phase(smem_u32(&sh.op_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
           const uint32_t full = smem_u32(&sh.b_full[sl.idx]);
           pend_mask |= 1u << sl.idx;
           pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
-          const uint32_t dst = smem_u32(ring_b + sl.idx * kBBytes);
-          if (p.b_mode == 1) {
-            // dgrad: b_rows tokens x 64 columns, K-major rows of 128 bytes
-            mbar_arrive_expect_tx(full, p.b_rows * 128);
-            tma_load_2d(dst, &tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + half);
-          } else if (p.b_mode == 2) {
-            // wgrad: b_rows swizzle atoms x 64 tokens x 64 columns
-            mbar_arrive_expect_tx(full, p.b_rows * kBoxBytes);
-            tma_load_3d(dst, &tm_g, full, 0, ti.r0 + kb * kTileK, (ti.nt * kTileN + half) / 64);
-          } else {
-            // wgrad, N not a multiple of 64: two 64 x 64 boxes (the second may lie past N)
-            mbar_arrive_expect_tx(full, 2 * kBoxBytes);
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d(dst + j * kBoxBytes, &tm_g, full, ti.nt * kTileN + half + 64 * j, ti.r0 + kb * kTileK);
+          const int nk = min(kUnitKb, ti.kblocks - kUnitKb * j);
+          mbar_arrive_expect_tx(full, nk * kb_bytes);
+          for (int h = 0; h < nk; ++h) {
+            const int kb = kUnitKb * j + h;
+            const uint32_t dst = smem_u32(ring_b + sl.idx * kBUnitBytes + h * kBBytes);
+            if (p.b_mode == 1) {
+              // dgrad: b_rows tokens x 64 columns, K-major rows of 128 bytes
+              tma_load_2d(dst, &tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + half);
+            } else if (p.b_mode == 2) {
+              // wgrad: b_rows swizzle atoms x 64 tokens x 64 columns
+              tma_load_3d(dst, &tm_g, full, 0, ti.r0 + kb * kTileK, (ti.nt * kTileN + half) / 64);
+            } else {
+              // wgrad, N not a multiple of 64: two 64 x 64 boxes (the second may lie past N)
+              for (int b = 0; b < 2; ++b)
+                tma_load_2d(dst + b * kBoxBytes, &tm_g, full, ti.nt * kTileN + half + 64 * b, ti.r0 + kb * kTileK);
+            }
           }
         }
         if (!ok) break;
       }
-      if (*abort_flag) drain_pending<kBStages>(sh.b_full, pend_mask, pend_par, limit);
+      if (*abort_flag) drain_pending<kUStages>(sh.b_full, pend_mask, pend_par, limit);
     }
   } else if (warp == 1) {
     // ===== MMA issuer: one thread of the even CTA drives the pair =====
-    // This thread shares its scheduler with busy dequant warps, so its per-k-block path is
-    // kept short: ring positions advance incrementally and the shared-memory descriptors
-    // are formed by adding to the 14-bit start-address field (addresses < 256 KB).
+    // This thread shares its scheduler with busy dequant warps, so its per-unit path is
+    // kept short: one barrier wait, eight MMAs and one commit per unit of two k-blocks;
+    // ring positions advance incrementally and the shared-memory descriptors are formed
+    // by adding to the 14-bit start-address field (addresses < 256 KB).
     if (lane == 0 && rank == 0) {
-      uint32_t ia = 0, pa = 0, ib = 0, pb = 0;   // ring slot and phase parity of the next k-block
-      int e_cur = 0;
+      uint32_t iu = 0, pu = 0;   // ring slot and phase parity of the next unit
+      ExpertCursor cur = cursor_begin<OP>(p);
       uint32_t acc = 0;
       const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), kBoxBytes, 1024);   // A: MN-major, atoms of 64 m at 8 KB
       const uint64_t bdesc0 = OP == kDgrad ? sdesc_sw128(smem_u32(ring_b), 16, 1024)          // B: K-major rows
                                            : sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B: MN-major
       constexpr uint32_t kAStep = 2048 >> 4;                          // 16 k-rows of an MN-major tile
       constexpr uint32_t kBStep = OP == kDgrad ? (32 >> 4) : (2048 >> 4);   // 16 k of the B tile
-      const uint32_t a_full0 = smem_u32(&sh.a_full[0]), a_empty0 = smem_u32(&sh.a_empty[0]);
-      const uint32_t b_empty0 = smem_u32(&sh.b_empty[0]);
-      // A k-block is ready once both CTAs' operand-ready arrivals are in: each dequant warp
-      // arrives only after it has seen its own CTA's grad_out half land, so the grad_out
-      // halves need no wait of their own here.
-      auto ready = [&](uint32_t sa, uint32_t qa) {
-        return wait_phase<true>(a_full0 + 8 * sa, qa, abort_flag, p.err, limit);
-      };
+      const uint32_t a_full0 = smem_u32(&sh.a_full[0]), op_empty0 = smem_u32(&sh.op_empty[0]);
+      // A unit is ready once every dequant warp of both CTAs has arrived: each arrives only
+      // after it has seen its own CTA's grad_out half land, so the grad_out halves need no
+      // wait of their own here.
+      auto ready = [&](uint32_t s, uint32_t q) { return wait_phase<true>(a_full0 + 8 * s, q, abort_flag, p.err, limit); };
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
+        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
         if (ti.kblocks == 0) continue;
         const uint32_t buf = acc & 1u;
         const uint32_t acc_phase = (acc >> 1) & 1u;
@@ -423,54 +443,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t n_mma = static_cast<uint32_t>(mma_width<OP>(ti.n_valid, p.b_mode));
         const uint32_t idesc = idesc_bf16_f32(kPair * kTileM, n_mma, true, OP == kWgrad);
         const uint32_t d_tmem = tmem_base + buf * kTileN;
-        // k-blocks go in rounds of two: eight MMAs, then the next round's operands are
-        // awaited while those MMAs are still queued, then the round's commits (a commit
-        // takes a slot of the tensor instruction queue; waiting after it would leave the
-        // pipe idle).  The next round's operand slots were released two rounds earlier,
-        // which needs at least four operand stages.
-        auto adv = [](uint32_t& i, uint32_t& ph, uint32_t n) {
-          if (++i == n) {
-            i = 0;
-            ph ^= 1u;
-          }
-        };
-        bool ok = ready(ia, pa);
-        if (ok && ti.kblocks > 1) {
-          uint32_t xa = ia, xpa = pa;
-          adv(xa, xpa, kAStages);
-          ok = ready(xa, xpa);
-        }
-        for (int kb = 0; ok && kb < ti.kblocks; kb += 2) {
-          const int nk = kb + 1 < ti.kblocks ? 2 : 1;
+        const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
+        // Each unit's MMAs are queued, then the next unit is awaited while they run, then
+        // the commit that frees the unit's slots (a commit takes a slot of the tensor
+        // instruction queue; waiting after it would leave the pipe idle).  The next unit's
+        // slots were freed by a commit issued at least one unit earlier.
+        bool ok = ready(iu, pu);
+        for (int j = 0; ok && j < units; ++j) {
+          const int nk = min(kUnitKb, ti.kblocks - kUnitKb * j);
           tc_fence_after();
-          uint32_t sa[2], sb[2];
+          const uint64_t ad = adesc0 + iu * (kAUnitBytes >> 4);
+          const uint64_t bd = bdesc0 + iu * (kBUnitBytes >> 4);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < kUnitKb; ++h) {
             if (h < nk) {
-              const uint64_t ad = adesc0 + ia * (kABytes >> 4);
-              const uint64_t bd = bdesc0 + ib * (kBBytes >> 4);
 #pragma unroll
               for (int kk = 0; kk < kTileK / 16; ++kk)
-                umma_bf16_pair(d_tmem, ad + kk * kAStep, bd + kk * kBStep, idesc, ((kb + h) | kk) != 0 ? 1u : 0u);
-              sa[h] = ia; sb[h] = ib;
-              adv(ia, pa, kAStages); adv(ib, pb, kBStages);
+                umma_bf16_pair(d_tmem, ad + h * (kABytes >> 4) + kk * kAStep, bd + h * (kBBytes >> 4) + kk * kBStep,
+                               idesc, (j | h | kk) != 0 ? 1u : 0u);
             }
           }
-          if (kb + 2 < ti.kblocks) {
-            ok = ready(ia, pa);
-            if (ok && kb + 3 < ti.kblocks) {
-              uint32_t xa = ia, xpa = pa;
-              adv(xa, xpa, kAStages);
-              ok = ready(xa, xpa);
-            }
+          const uint32_t su = iu;
+          if (++iu == kUStages) {
+            iu = 0;
+            pu ^= 1u;
           }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (h < nk) {
-              umma_commit_pair(a_empty0 + 8 * sa[h], kPairMask);
-              umma_commit_pair(b_empty0 + 8 * sb[h], kPairMask);
-            }
-          }
+          if (j + 1 < units) ok = ready(iu, pu);
+          umma_commit_pair(op_empty0 + 8 * su, kPairMask);
         }
         if (!ok) break;
         umma_commit_pair(smem_u32(&sh.tmem_full[buf]), kPairMask);
@@ -482,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp - 4;                  // TMEM lane quarter (warp % 4)
     const int i = q * 32 + lane;             // accumulator row = tile m index (permuted)
     const int mcol = lane_to_col<FMT>(i);
-    int e_cur = 0;
+    ExpertCursor cur = cursor_begin<OP>(p);
     uint32_t acc = 0;
     for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
+      const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
       const int m = ti.mt * kTileM + mcol;
       const bool mok = m < p.Kc;
       __nv_bfloat16* obase;
@@ -543,10 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 4; ++j)
       st_off[j] = (g >> 1) * kBoxBytes + r * 128 + ((((g & 1) * 4 + j) ^ (r & 7)) << 4);
     const uint32_t p_off = F::kFp4 ? r * F::kPRowBytes + 16 * g : r * F::kPRowBytes + 32 * g + 16 * (r & 1);
-    uint32_t kc = 0;                                           // k-blocks seen so far (all teams)
-    int e_cur = 0;
+    uint32_t uc = 0;   // units of earlier tiles: ring position of this tile's unit 0
+    ExpertCursor cur = cursor_begin<OP>(p);
     for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-      const TileInfo ti = decode_tile<OP>(t, e_cur, sh, p, rank);
+      const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
       const int m0 = ti.mt * kTileM;
       const int col0 = m0 + 32 * g;
       const bool col_ok = col0 < p.Kc;
@@ -556,13 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this thread's scale byte(s) inside the staged 16-byte scale window of a row
       const uint32_t s_off = F::kPBytes + r * 16 + (FMT == BSQ_MXFP4 ? ((m0 >> 5) & 15) + g : ((m0 >> 4) & 15) + 2 * g);
       bool ok = true;
-      for (int kb = 0; kb < ti.kblocks; ++kb, ++kc) {
-        if (static_cast<int>(kc % kDeqTeams) != team) continue;
-        const Slot sp = ring_slot<kPStages>(kc);
-        const Slot sa = ring_slot<kAStages>(kc);
+      const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
+      for (int j = 0; j < units; ++j) {
+        // This team's k-block of the unit.  Past the tile's last k-block the team only
+        // keeps the barrier counts: nothing is read or written and the MMA skips it.
+        const int kb = kUnitKb * j + team;
+        const bool present = kb < ti.kblocks;
+        const Slot sa = ring_slot<kUStages>(uc + j);
+        const Slot sp = ring_slot<F::kPUnits>(uc + j);
         const int prow0 = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
         const int kvalid = OP == kDgrad ? min(kTileK, p.N - kb * kTileK) : min(kTileK, ti.r1 - prow0);
-        const bool valid = r < kvalid && col_ok;
+        const bool valid = present && r < kvalid && col_ok;
+        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
         // Scales that do not come through TMA are fetched before the wait.
         uint32_t sraw = 0;
         float sf = 0.f;
@@ -577,11 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             sraw = static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4))) |
                    (static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
         }
+        // Both teams wait on every phase of the packed slot (in unit order) and both count
+        // out of it, present or not.
         ok = wait_phase(smem_u32(&sh.p_full[sp.idx]), sp.par, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         // ---- read this thread's packed bytes (and scale) out of the packed ring
-        const uint32_t pst = p_ring + sp.idx * F::kPStageBytes;
+        const uint32_t pst = p_ring + sp.idx * F::kPUnitBytes + team * F::kPStageBytes;
         uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
         if (FMT != BSQ_BF16 && valid) {
           if (F::kFp4) {
@@ -598,8 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
-        if (FMT == BSQ_BF16) {
+        if (FMT == BSQ_BF16 && present) {
           // BF16 operand: the TMA tile is already in the swizzled layout; copy this
           // thread's four 16-byte chunks (zero outside the contraction).
 #pragma unroll
@@ -609,82 +614,87 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));   // packed slot free
-        // ---- decode into the BF16 operand ring
-        if (FMT != BSQ_BF16) {
-          if (valid) {
-            if (F::kFp4) {
-              spread_e2m1x8(wa.x, v[0]);
-              spread_e2m1x8(wa.y, v[1]);
-              spread_e2m1x8(wa.z, v[2]);
-              spread_e2m1x8(wa.w, v[3]);
-              ScaleBf16 s0, s1;
-              if (FMT == BSQ_MXFP4) {
-                s0 = make_scale_e8m0(sraw);
-                s1 = s0;
-              } else {
-                s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
-                s1 = make_scale_nvfp4(sraw >> 8, tscale);
-              }
-              if (s0.fast && s1.fast) {
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));   // this warp is done with the packed slot
+        if (present) {
+          // ---- decode into the BF16 operand ring
+          if (FMT != BSQ_BF16) {
+            if (valid) {
+              if (F::kFp4) {
+                spread_e2m1x8(wa.x, v[0]);
+                spread_e2m1x8(wa.y, v[1]);
+                spread_e2m1x8(wa.z, v[2]);
+                spread_e2m1x8(wa.w, v[3]);
+                ScaleBf16 s0, s1;
+                if (FMT == BSQ_MXFP4) {
+                  s0 = make_scale_e8m0(sraw);
+                  s1 = s0;
+                } else {
+                  s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
+                  s1 = make_scale_nvfp4(sraw >> 8, tscale);
+                }
+                if (s0.fast && s1.fast) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  v[0][i] = bf16x2_mul(v[0][i], s0.c2);
-                  v[1][i] = bf16x2_mul(v[1][i], s0.c2);
-                  v[2][i] = bf16x2_mul(v[2][i], s1.c2);
-                  v[3][i] = bf16x2_mul(v[3][i], s1.c2);
+                  for (int i = 0; i < 4; ++i) {
+                    v[0][i] = bf16x2_mul(v[0][i], s0.c2);
+                    v[1][i] = bf16x2_mul(v[1][i], s0.c2);
+                    v[2][i] = bf16x2_mul(v[2][i], s1.c2);
+                    v[3][i] = bf16x2_mul(v[3][i], s1.c2);
+                  }
+                } else {
+                  scale_pairs4(v[0], s0, kPow2_126x2);
+                  scale_pairs4(v[1], s0, kPow2_126x2);
+                  scale_pairs4(v[2], s1, kPow2_126x2);
+                  scale_pairs4(v[3], s1, kPow2_126x2);
                 }
               } else {
-                scale_pairs4(v[0], s0, kPow2_126x2);
-                scale_pairs4(v[1], s0, kPow2_126x2);
-                scale_pairs4(v[2], s1, kPow2_126x2);
-                scale_pairs4(v[3], s1, kPow2_126x2);
+                const ScaleBf16 s0 = make_scale_fp8(sf);
+                decode_e4m3x8(wa.x, wa.y, s0, v[0]);
+                decode_e4m3x8(wa.z, wa.w, s0, v[1]);
+                decode_e4m3x8(wb.x, wb.y, s0, v[2]);
+                decode_e4m3x8(wb.z, wb.w, s0, v[3]);
               }
             } else {
-              const ScaleBf16 s0 = make_scale_fp8(sf);
-              decode_e4m3x8(wa.x, wa.y, s0, v[0]);
-              decode_e4m3x8(wa.z, wa.w, s0, v[1]);
-              decode_e4m3x8(wb.x, wb.y, s0, v[2]);
-              decode_e4m3x8(wb.z, wb.w, s0, v[3]);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[j][i] = 0u;
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) v[j][i] = 0u;
           }
         }
-        ok = wait_phase(smem_u32(&sh.a_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
+        // The unit's operand and grad_out slots are free once its previous MMAs completed.
+        ok = wait_phase(smem_u32(&sh.op_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
-        // 16-byte slot (4(g&1) + j) XOR (r & 7)
-        const uint32_t ast = a_ring + sa.idx * kABytes;
+        if (present) {
+          // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
+          // 16-byte slot (4(g&1) + j) XOR (r & 7)
+          const uint32_t ast = a_ring + sa.idx * kAUnitBytes + team * kABytes;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sts128(ast + st_off[j], v[j][0], v[j][1], v[j][2], v[j][3]);
-        // This CTA's grad_out half must have landed before the operand-ready arrival: the
-        // even CTA's MMA thread only watches its own half's bytes.
-        const Slot sb = ring_slot<kBStages>(kc);
-        ok = wait_phase(smem_u32(&sh.b_full[sb.idx]), sb.par, abort_flag, p.err, limit);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        if (OP == kWgrad && kvalid < kTileK) {
-          // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must not
-          // reach the products: zero them in both boxes of this CTA's half.
-          const uint32_t b_tile = smem_u32(ring_b + sb.idx * kBBytes);
-          const int dt = dw * 32 + lane;
-          for (int idx = dt; idx < (kTileK - kvalid) * 8 * 2; idx += 256) {
-            const int box = idx / ((kTileK - kvalid) * 8);
-            const int rem = idx % ((kTileK - kvalid) * 8);
-            const int rr = kvalid + rem / 8, c = rem % 8;
-            sts128(b_tile + box * kBoxBytes + rr * 128 + c * 16, 0u, 0u, 0u, 0u);
+          for (int j = 0; j < 4; ++j) sts128(ast + st_off[j], v[j][0], v[j][1], v[j][2], v[j][3]);
+          // This CTA's grad_out half must have landed before the operand-ready arrival: the
+          // even CTA's MMA thread only watches the arrivals.
+          ok = wait_phase(smem_u32(&sh.b_full[sa.idx]), sa.par, abort_flag, p.err, limit);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          if (OP == kWgrad && kvalid < kTileK) {
+            // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must
+            // not reach the products: zero them in both boxes of this CTA's half.
+            const uint32_t b_tile = smem_u32(ring_b + sa.idx * kBUnitBytes + team * kBBytes);
+            const int dt = dw * 32 + lane;
+            for (int idx = dt; idx < (kTileK - kvalid) * 8 * 2; idx += 256) {
+              const int box = idx / ((kTileK - kvalid) * 8);
+              const int rem = idx % ((kTileK - kvalid) * 8);
+              const int rr = kvalid + rem / 8, c = rem % 8;
+              sts128(b_tile + box * kBoxBytes + rr * 128 + c * 16, 0u, 0u, 0u, 0u);
+            }
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive_rank(smem_u32(&sh.a_full[sa.idx]), 0);
       }
       if (!ok) break;
+      uc += units;
     }
   }
 
@@ -834,6 +844,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   // Upper bound of the pair-tile count (the exact count depends on the offsets, read on the device).
   const int64_t nn = (a.N + kTileN - 1) / kTileN;
   const int64_t bound = OP == kDgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
+  static_assert(F::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
   auto kern = bsq_gemm_kernel<FMT, OP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
