@@ -126,11 +126,20 @@ __device__ __forceinline__ void decode_e2m1x8(uint32_t w, const ScaleBf16& s, ui
   scale_pairs4(out, s, kPow2_126x2);
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 // Scaled-down BF16 pairs of 4 E4M3 codes (one word, element j in byte j):
 // a = (c0, c2), b = (c1, c3), each = code value * 2^-120 (NaN codes not handled here).
+// prmt puts each code in the low byte of its 16-bit half with a sign-filled byte above
+// it; a 4-bit shift then lands the code's 7 magnitude bits (eeee.mmm) on BF16 bits 10..4
+// and a sign copy on bit 15, and the mask clears the rest.
 __device__ __forceinline__ void spread_e4m3x4(uint32_t w, uint32_t& a, uint32_t& b) {
-  a = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);
-  b = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);
+  a = (prmt(w, 0u, 0xA280u) << 4) & 0x87F087F0u;
+  b = (prmt(w, 0u, 0xB391u) << 4) & 0x87F087F0u;
 }
 
 __device__ __forceinline__ bool e4m3_any_nan(uint32_t w) {
@@ -166,10 +175,31 @@ __device__ __forceinline__ void decode_e4m3x8(uint32_t w0, uint32_t w1, const Sc
   }
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
+// 32 E4M3 codes of one row (lo = codes 0..15, hi = codes 16..31, element j of a word in
+// byte j) -> groups out[g] = decode_e4m3x8 of codes 8g..8g+7, scaled; one NaN test covers
+// all 32 codes (an OR can only add candidates, the fix checks each byte).
+__device__ __forceinline__ void decode_e4m3x32(const uint4& lo, const uint4& hi, const ScaleBf16& s,
+                                               uint32_t (&out)[4][4]) {
+  spread_e4m3x4(lo.x, out[0][0], out[0][1]);
+  spread_e4m3x4(lo.y, out[0][2], out[0][3]);
+  spread_e4m3x4(lo.z, out[1][0], out[1][1]);
+  spread_e4m3x4(lo.w, out[1][2], out[1][3]);
+  spread_e4m3x4(hi.x, out[2][0], out[2][1]);
+  spread_e4m3x4(hi.y, out[2][2], out[2][3]);
+  spread_e4m3x4(hi.z, out[3][0], out[3][1]);
+  spread_e4m3x4(hi.w, out[3][2], out[3][3]);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) scale_pairs4(out[g], s, kPow2_120x2);
+  if (e4m3_any_nan(lo.x | lo.y | lo.z | lo.w | hi.x | hi.y | hi.z | hi.w)) {
+    e4m3_fix_nan(lo.x, out[0][0], out[0][1]);
+    e4m3_fix_nan(lo.y, out[0][2], out[0][3]);
+    e4m3_fix_nan(lo.z, out[1][0], out[1][1]);
+    e4m3_fix_nan(lo.w, out[1][2], out[1][3]);
+    e4m3_fix_nan(hi.x, out[2][0], out[2][1]);
+    e4m3_fix_nan(hi.y, out[2][2], out[2][3]);
+    e4m3_fix_nan(hi.z, out[3][0], out[3][1]);
+    e4m3_fix_nan(hi.w, out[3][2], out[3][3]);
+  }
 }
 
 // Undo the pair permutation: pairs (x_lo, x_hi),(y_lo, y_hi) -> (x_lo, y_lo),(x_hi, y_hi).

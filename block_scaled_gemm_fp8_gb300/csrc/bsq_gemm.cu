@@ -534,13 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qtr = lane >> 3;
     const int r = dw * 8 + (qtr & 1) * 4 + (lane & 3);          // 0..63
     const int g = (qtr >> 1) * 2 + ((lane >> 2) & 1);           // 0..3
-    // Shared addresses that do not change between k-blocks: the four swizzled 16-byte
-    // store slots of this thread inside an A stage, and its packed bytes inside a P stage.
+    // Shared addresses that do not change between k-blocks: the swizzled 16-byte store
+    // slot of decoded group j (8 elements) of this thread inside an A stage, and its packed
+    // bytes inside a P stage.  FP8 odd rows read their second 16 codes first (bank
+    // spread), so their groups 0,1 hold chunks 2,3 of the row's 32 columns and vice versa.
     const uint32_t a_ring = smem_u32(ring_a), p_ring = smem_u32(ring_p);
     uint32_t st_off[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      st_off[j] = (g >> 1) * kBoxBytes + r * 128 + ((((g & 1) * 4 + j) ^ (r & 7)) << 4);
+    for (int j = 0; j < 4; ++j) {
+      const int chunk = (FMT == BSQ_FP8_E4M3_B128 && (r & 1)) ? (j ^ 2) : j;
+      st_off[j] = (g >> 1) * kBoxBytes + r * 128 + ((((g & 1) * 4 + chunk) ^ (r & 7)) << 4);
+    }
     const uint32_t p_off = F::kFp4 ? r * F::kPRowBytes + 16 * g : r * F::kPRowBytes + 32 * g + 16 * (r & 1);
     uint32_t uc = 0;   // units of earlier tiles: ring position of this tile's unit 0
     ExpertCursor cur = cursor_begin<OP>(p);
@@ -595,13 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             wa = lds128(pst + p_off);
           } else {
             // rows 128 bytes apart share banks: odd rows read their second half first
+            // (the store slots above put the groups back in place)
             wa = lds128(pst + p_off);
             wb = lds128(pst + (p_off ^ 16u));
-            if (r & 1) {
-              const uint4 tmp = wa;
-              wa = wb;
-              wb = tmp;
-            }
           }
         }
         if (FMT == BSQ_BF16 && present) {
@@ -647,11 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   scale_pairs4(v[3], s1, kPow2_126x2);
                 }
               } else {
-                const ScaleBf16 s0 = make_scale_fp8(sf);
-                decode_e4m3x8(wa.x, wa.y, s0, v[0]);
-                decode_e4m3x8(wa.z, wa.w, s0, v[1]);
-                decode_e4m3x8(wb.x, wb.y, s0, v[2]);
-                decode_e4m3x8(wb.z, wb.w, s0, v[3]);
+                decode_e4m3x32(wa, wb, make_scale_fp8(sf), v);
               }
             } else {
 #pragma unroll
