@@ -426,7 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), kBoxBytes, 1024);   // A: MN-major, atoms of 64 m at 8 KB
       const uint64_t bdesc0 = OP == kDgrad ? sdesc_sw128(smem_u32(ring_b), 16, 1024)          // B: K-major rows
                                            : sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B: MN-major
-      constexpr uint32_t kAStep = 2048 >> 4;                          // 16 k-rows of an MN-major tile
       constexpr uint32_t kBStep = OP == kDgrad ? (32 >> 4) : (2048 >> 4);   // 16 k of the B tile
       const uint32_t a_full0 = smem_u32(&sh.a_full[0]), op_empty0 = smem_u32(&sh.op_empty[0]);
       // A unit is ready once every dequant warp of both CTAs has arrived: each arrives only
@@ -457,10 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < kUnitKb; ++h) {
             if (h < nk) {
-#pragma unroll
-              for (int kk = 0; kk < kTileK / 16; ++kk)
-                umma_bf16_pair(d_tmem, ad + h * (kABytes >> 4) + kk * kAStep, bd + h * (kBBytes >> 4) + kk * kBStep,
-                               idesc, (j | h | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair_k64<kBStep>(d_tmem, ad + h * (kABytes >> 4), bd + h * (kBBytes >> 4), idesc,
+                                         (j | h) != 0 ? 1u : 0u);
             }
           }
           const uint32_t su = iu;

@@ -161,13 +161,24 @@ __device__ __forceinline__ void tc_fence_after() {
 // D[tmem] (+)= A[smem] * B[smem] with BF16 inputs and FP32 accumulation, M = 256.  Each CTA
 // supplies 128 rows of A and N/2 rows of B (CTA r: B rows [r*N/2, (r+1)*N/2)) at the same
 // shared offsets, and receives its 128 rows of D (all N columns) in its own TMEM.
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
+// This issues the four MMAs of one 64-deep k-block: A advances 2 KB (16 k-rows of an
+// MN-major tile) and B by BSTEP descriptor units per 16 k.  The first MMA accumulates when
+// `accumulate` is set, the other three always.  One asm block keeps the issuing thread's
+// path short: the descriptor steps are immediates and one predicate is formed.
+template <uint32_t BSTEP>
+__device__ __forceinline__ void umma_bf16_pair_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "setp.eq.b32 q, %4, %4;\n\t"
+      "add.s64 a1, %1, 128;\n\tadd.s64 a2, %1, 256;\n\tadd.s64 a3, %1, 384;\n\t"
+      "add.s64 b1, %2, %5;\n\tadd.s64 b2, %2, %6;\n\tadd.s64 b3, %2, %7;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP)
       : "memory");
 }
 // Arrive once on the barrier at the same offset in every CTA of `mask` when every pair MMA
