@@ -47,6 +47,7 @@
 // bounded by %globaltimer and records a timeout in the device error word (and stops the
 // peer CTA) instead of hanging.
 #include <cuda_bf16.h>
+#include <cstdlib>
 #include <cudaTypedefs.h>
 
 #include "bsq_decode.cuh"
@@ -58,8 +59,24 @@ namespace bsq {
 
 namespace {
 
-constexpr int kDeqTeams = 2;                    // dequant teams alternate k-blocks
-constexpr int kThreads = 256 + kDeqTeams * 256;  // 8 control/epilogue warps + 8 warps per team
+constexpr int kDeqTeams = 2;                    // dequant team t fills k-block t of every unit
+constexpr int kThreads = 768;                    // 4 control warps, epilogue and dequant warps
+
+// Warp roles.  The default kernel has 4 epilogue warps (one per TMEM lane quarter) and two
+// dequant teams of 8 warps, each thread decoding one row of its team's k-block.  The
+// short-tile kernel (grouped wgrad with few rows per expert, where a tile has a handful of
+// k-blocks and its epilogue sets the pace) has 12 epilogue warps, three per lane quarter
+// splitting the columns, and two teams of 4 dequant warps decoding two rows per thread.
+template <bool SHORT>
+struct Roles {
+  static constexpr int kEpiWarps = SHORT ? 12 : 4;
+  static constexpr int kEpiPerQuarter = kEpiWarps / 4;
+  static constexpr int kDeqPerTeam = SHORT ? 4 : 8;
+  static constexpr int kRows = 8 / kDeqPerTeam;        // k-block rows decoded per dequant thread
+  static constexpr int kRowStep = 8 * kDeqPerTeam;     // distance between a thread's rows
+  static constexpr int kFirstDeq = 4 + kEpiWarps;
+  static_assert(kFirstDeq + kDeqTeams * kDeqPerTeam == kThreads / 32, "every warp has a role");
+};
 constexpr int kBoxBytes = 64 * 64 * 2;          // one 64x64 BF16 box = one swizzle column of 64 rows
 constexpr int kABytes = kTileM * kTileK * 2;     // 16 KB: dequantized operand, 2 swizzle columns
 constexpr int kPair = 2;                         // CTAs of one 2-SM MMA (a cluster)
@@ -243,6 +260,50 @@ __device__ __forceinline__ int lane_to_col(int i) {
   return i;
 }
 
+// This thread's 32 packed codes of one k-block row (FP8: wa = codes 0..15 as read, wb the
+// other 16; FP4: wa) -> 4 groups of 4 BF16 pairs, scaled; zeros outside the operand.
+template <int FMT>
+__device__ __forceinline__ void decode_row(const uint4& wa, const uint4& wb, uint32_t sraw, float sf, float tscale,
+                                           bool valid, uint32_t (&v)[4][4]) {
+  if (!valid) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[j][i] = 0u;
+    return;
+  }
+  if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) {
+    spread_e2m1x8(wa.x, v[0]);
+    spread_e2m1x8(wa.y, v[1]);
+    spread_e2m1x8(wa.z, v[2]);
+    spread_e2m1x8(wa.w, v[3]);
+    ScaleBf16 s0, s1;
+    if (FMT == BSQ_MXFP4) {
+      s0 = make_scale_e8m0(sraw);
+      s1 = s0;
+    } else {
+      s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
+      s1 = make_scale_nvfp4(sraw >> 8, tscale);
+    }
+    if (s0.fast && s1.fast) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[0][i] = bf16x2_mul(v[0][i], s0.c2);
+        v[1][i] = bf16x2_mul(v[1][i], s0.c2);
+        v[2][i] = bf16x2_mul(v[2][i], s1.c2);
+        v[3][i] = bf16x2_mul(v[3][i], s1.c2);
+      }
+    } else {
+      scale_pairs4(v[0], s0, kPow2_126x2);
+      scale_pairs4(v[1], s0, kPow2_126x2);
+      scale_pairs4(v[2], s1, kPow2_126x2);
+      scale_pairs4(v[3], s1, kPow2_126x2);
+    }
+  } else if (FMT == BSQ_FP8_E4M3_B128) {
+    decode_e4m3x32(wa, wb, make_scale_fp8(sf), v);
+  }
+}
+
 // Let the TMA copies this thread issued into the given slots land (orderly abort).
 template <int N>
 __device__ __forceinline__ void drain_pending(uint64_t* full, uint32_t mask, uint32_t par, uint64_t limit) {
@@ -254,11 +315,13 @@ __device__ __forceinline__ void drain_pending(uint64_t* full, uint32_t mask, uin
     }
 }
 
-template <int FMT, int OP>
+template <int FMT, int OP, bool SHORT>
 __global__ void __launch_bounds__(kThreads, 1)
     bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_g,
                     const __grid_constant__ CUtensorMap tm_s, const Params p) {
   using F = Fmt<FMT>;
+  using R = Roles<SHORT>;
+  static_assert(!SHORT || FMT != BSQ_BF16, "the short-tile kernel decodes packed formats only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring_b = smem;
@@ -275,16 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < F::kPUnits; ++s) {
       mbar_init(smem_u32(&sh.p_full[s]), 1);
-      mbar_init(smem_u32(&sh.p_empty[s]), 8 * kDeqTeams);   // every dequant warp of this CTA
+      mbar_init(smem_u32(&sh.p_empty[s]), R::kDeqPerTeam * kDeqTeams);   // every dequant warp of this CTA
     }
     for (int s = 0; s < kUStages; ++s) {
-      mbar_init(smem_u32(&sh.a_full[s]), 8 * kDeqTeams * kPair);   // every dequant warp of both CTAs (even CTA's is used)
+      mbar_init(smem_u32(&sh.a_full[s]), R::kDeqPerTeam * kDeqTeams * kPair);   // every dequant warp of both CTAs (even CTA's is used)
       mbar_init(smem_u32(&sh.op_empty[s]), 1);
       mbar_init(smem_u32(&sh.b_full[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sh.tmem_full[b]), 1);
-      mbar_init(smem_u32(&sh.tmem_empty[b]), 4 * kPair);   // epilogue warps of both CTAs
+      mbar_init(smem_u32(&sh.tmem_empty[b]), R::kEpiWarps * kPair);   // epilogue warps of both CTAs
     }
     mbar_init(smem_u32(&sh.drain), 1);
     sh.abort_flag = 0u;
@@ -473,10 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++acc;
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 4 + R::kEpiWarps) {
     // ===== epilogue =====
-    const int q = warp - 4;                  // TMEM lane quarter (warp % 4)
-    const int i = q * 32 + lane;             // accumulator row = tile m index (permuted)
+    // Warp w reads TMEM lane quarter w % 4; the kEpiPerQuarter warps of a quarter take its
+    // 32-column chunks in turn.
+    const int q = warp & 3;                   // TMEM lane quarter
+    const int sub = R::kEpiPerQuarter > 1 ? (warp - 4) >> 2 : 0;   // 0 .. kEpiPerQuarter-1
+    const int i = q * 32 + lane;              // accumulator row = tile m index (permuted)
     const int mcol = lane_to_col<FMT>(i);
     ExpertCursor cur = cursor_begin<OP>(p);
     uint32_t acc = 0;
@@ -493,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // wgrad of an expert without rows: exact zeros
         const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
         if (mok)
-          for (int n = 0; n < ti.n_valid; ++n) obase[static_cast<int64_t>(n) * p.Kc] = z;
+          for (int n = sub; n < ti.n_valid; n += R::kEpiPerQuarter) obase[static_cast<int64_t>(n) * p.Kc] = z;
         continue;
       }
       const uint32_t buf = acc & 1u;
@@ -504,11 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int nchunks = (ti.n_valid + 31) >> 5;
-      for (int c = 0; c < nchunks; ++c) {
+      if (sub >= nchunks) {
+        // no chunk for this warp: release the accumulator at once
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_rank(smem_u32(&sh.tmem_empty[buf]), 0);
+      }
+      for (int c = sub; c < nchunks; c += R::kEpiPerQuarter) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + c * 32, v);
         tmem_wait_ld();
-        if (c == nchunks - 1) {
+        if (c + R::kEpiPerQuarter >= nchunks) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_rank(smem_u32(&sh.tmem_empty[buf]), 0);   // the even CTA's MMA reuses it
@@ -521,20 +593,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= R::kFirstDeq) {
     // ===== dequantization =====
-    // Thread -> (row r of the k-block, group g of 32 columns).  A quarter-warp covers 4
-    // consecutive rows x 2 groups, so its 16-byte stores into the swizzled tile hit 8
-    // distinct bank groups; each thread needs one MX scale (two NVFP4, one FP8 block).
-    const int team = (warp - 8) >> 3;
-    const int dw = (warp - 8) & 7;                             // 0..7 within the team
+    // Thread -> (row r of the k-block, group g of 32 columns), plus rows r + kRowStep when
+    // a thread decodes kRows rows.  A quarter-warp covers 4 consecutive rows x 2 groups,
+    // so its 16-byte stores into the swizzled tile hit 8 distinct bank groups; each thread
+    // needs one MX scale per row (two NVFP4, one FP8 block).
+    const int dq = warp - R::kFirstDeq;
+    const int team = dq / R::kDeqPerTeam;
+    const int dw = dq % R::kDeqPerTeam;                        // warp within the team
     const int qtr = lane >> 3;
-    const int r = dw * 8 + (qtr & 1) * 4 + (lane & 3);          // 0..63
+    const int r = dw * 8 + (qtr & 1) * 4 + (lane & 3);          // 0 .. kRowStep-1
     const int g = (qtr >> 1) * 2 + ((lane >> 2) & 1);           // 0..3
     // Shared addresses that do not change between k-blocks: the swizzled 16-byte store
-    // slot of decoded group j (8 elements) of this thread inside an A stage, and its packed
-    // bytes inside a P stage.  FP8 odd rows read their second 16 codes first (bank
-    // spread), so their groups 0,1 hold chunks 2,3 of the row's 32 columns and vice versa.
+    // slot of decoded group j (8 elements) of row r inside an A stage, and its packed
+    // bytes inside a P stage (rows r + kRowStep: plus kRowStep rows; the swizzle phase
+    // r & 7 is the same).  FP8 odd rows read their second 16 codes first (bank spread),
+    // so their groups 0,1 hold chunks 2,3 of the row's 32 columns and vice versa.
     const uint32_t a_ring = smem_u32(ring_a), p_ring = smem_u32(ring_p);
     uint32_t st_off[4];
 #pragma unroll
@@ -553,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pbatch = OP == kDgrad ? ti.e : 0;
       float tscale = 0.f;
       if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + pbatch);
-      // this thread's scale byte(s) inside the staged 16-byte scale window of a row
+      // this thread's scale byte(s) inside the staged 16-byte scale window of row r
       const uint32_t s_off = F::kPBytes + r * 16 + (FMT == BSQ_MXFP4 ? ((m0 >> 5) & 15) + g : ((m0 >> 4) & 15) + 2 * g);
       bool ok = true;
       const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
@@ -566,104 +641,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Slot sp = ring_slot<F::kPUnits>(uc + j);
         const int prow0 = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
         const int kvalid = OP == kDgrad ? min(kTileK, p.N - kb * kTileK) : min(kTileK, ti.r1 - prow0);
-        const bool valid = present && r < kvalid && col_ok;
-        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
+        bool valid[R::kRows];
         // Scales that do not come through TMA are fetched before the wait.
-        uint32_t sraw = 0;
-        float sf = 0.f;
-        if (valid) {
-          const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + r;
-          if (FMT == BSQ_FP8_E4M3_B128)
-            sf = __ldg(reinterpret_cast<const float*>(p.scale) +
-                       (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + r) >> 7)) * p.scale_ld + (col0 >> 7));
-          else if (FMT == BSQ_MXFP4 && !p.scale_tma)
-            sraw = __ldg(p.scale + grow * p.scale_ld + (col0 >> 5));
-          else if (FMT == BSQ_NVFP4 && !p.scale_tma)
-            sraw = static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4))) |
-                   (static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
+        uint32_t sraw[R::kRows];
+        float sf[R::kRows];
+#pragma unroll
+        for (int ps = 0; ps < R::kRows; ++ps) {
+          const int rr = r + ps * R::kRowStep;
+          valid[ps] = present && rr < kvalid && col_ok;
+          sraw[ps] = 0;
+          sf[ps] = 0.f;
+          if (valid[ps]) {
+            const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + rr;
+            if (FMT == BSQ_FP8_E4M3_B128)
+              sf[ps] = __ldg(reinterpret_cast<const float*>(p.scale) +
+                             (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + rr) >> 7)) * p.scale_ld +
+                             (col0 >> 7));
+            else if (FMT == BSQ_MXFP4 && !p.scale_tma)
+              sraw[ps] = __ldg(p.scale + grow * p.scale_ld + (col0 >> 5));
+            else if (FMT == BSQ_NVFP4 && !p.scale_tma)
+              sraw[ps] = static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4))) |
+                         (static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
+          }
         }
         // Both teams wait on every phase of the packed slot (in unit order) and both count
         // out of it, present or not.
         ok = wait_phase(smem_u32(&sh.p_full[sp.idx]), sp.par, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        // ---- read this thread's packed bytes (and scale) out of the packed ring
+        // ---- read this thread's packed bytes (and scales) out of the packed ring
         const uint32_t pst = p_ring + sp.idx * F::kPUnitBytes + team * F::kPStageBytes;
-        uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
-        if (FMT != BSQ_BF16 && valid) {
-          if (F::kFp4) {
-            if (p.scale_tma) sraw = FMT == BSQ_MXFP4 ? lds_u8(pst + s_off) : lds_u16(pst + s_off);
-            wa = lds128(pst + p_off);
-          } else {
-            // rows 128 bytes apart share banks: odd rows read their second half first
-            // (the store slots above put the groups back in place)
-            wa = lds128(pst + p_off);
-            wb = lds128(pst + (p_off ^ 16u));
+        uint4 wa[R::kRows], wb[R::kRows];
+        uint32_t v[4][4];   // 4 groups of 8 elements, 4 BF16 pairs each (permuted inside the group)
+#pragma unroll
+        for (int ps = 0; ps < R::kRows; ++ps) {
+          wa[ps] = make_uint4(0, 0, 0, 0);
+          wb[ps] = make_uint4(0, 0, 0, 0);
+          const uint32_t po = p_off + ps * R::kRowStep * F::kPRowBytes;
+          if (FMT != BSQ_BF16 && valid[ps]) {
+            if (F::kFp4) {
+              if (p.scale_tma) {
+                const uint32_t so = s_off + ps * R::kRowStep * 16;
+                sraw[ps] = FMT == BSQ_MXFP4 ? lds_u8(pst + so) : lds_u16(pst + so);
+              }
+              wa[ps] = lds128(pst + po);
+            } else {
+              // rows 128 bytes apart share banks: odd rows read their second half first
+              // (the store slots above put the groups back in place)
+              wa[ps] = lds128(pst + po);
+              wb[ps] = lds128(pst + (po ^ 16u));
+            }
           }
         }
         if (FMT == BSQ_BF16 && present) {
           // BF16 operand: the TMA tile is already in the swizzled layout; copy this
           // thread's four 16-byte chunks (zero outside the contraction).
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 c = r < kvalid ? lds128(pst + st_off[j]) : make_uint4(0, 0, 0, 0);
-            v[j][0] = c.x; v[j][1] = c.y; v[j][2] = c.z; v[j][3] = c.w;
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint4 c = r < kvalid ? lds128(pst + st_off[jj]) : make_uint4(0, 0, 0, 0);
+            v[jj][0] = c.x; v[jj][1] = c.y; v[jj][2] = c.z; v[jj][3] = c.w;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));   // this warp is done with the packed slot
-        if (present) {
-          // ---- decode into the BF16 operand ring
-          if (FMT != BSQ_BF16) {
-            if (valid) {
-              if (F::kFp4) {
-                spread_e2m1x8(wa.x, v[0]);
-                spread_e2m1x8(wa.y, v[1]);
-                spread_e2m1x8(wa.z, v[2]);
-                spread_e2m1x8(wa.w, v[3]);
-                ScaleBf16 s0, s1;
-                if (FMT == BSQ_MXFP4) {
-                  s0 = make_scale_e8m0(sraw);
-                  s1 = s0;
-                } else {
-                  s0 = make_scale_nvfp4(sraw & 0xFFu, tscale);
-                  s1 = make_scale_nvfp4(sraw >> 8, tscale);
-                }
-                if (s0.fast && s1.fast) {
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    v[0][i] = bf16x2_mul(v[0][i], s0.c2);
-                    v[1][i] = bf16x2_mul(v[1][i], s0.c2);
-                    v[2][i] = bf16x2_mul(v[2][i], s1.c2);
-                    v[3][i] = bf16x2_mul(v[3][i], s1.c2);
-                  }
-                } else {
-                  scale_pairs4(v[0], s0, kPow2_126x2);
-                  scale_pairs4(v[1], s0, kPow2_126x2);
-                  scale_pairs4(v[2], s1, kPow2_126x2);
-                  scale_pairs4(v[3], s1, kPow2_126x2);
-                }
-              } else {
-                decode_e4m3x32(wa, wb, make_scale_fp8(sf), v);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[j][i] = 0u;
-            }
-          }
-        }
+        // ---- decode the first row into registers while the operand slot may still be busy
+        if (FMT != BSQ_BF16 && present) decode_row<FMT>(wa[0], wb[0], sraw[0], sf[0], tscale, valid[0], v);
         // The unit's operand and grad_out slots are free once its previous MMAs completed.
         ok = wait_phase(smem_u32(&sh.op_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         if (present) {
-          // group j of this thread = 8-element chunk 4g + j of the row: swizzle column g/2,
-          // 16-byte slot (4(g&1) + j) XOR (r & 7)
+          // group jj of this thread = 8-element chunk 4g + jj of the row: swizzle column
+          // g/2, 16-byte slot (4(g&1) + jj) XOR (r & 7)
           const uint32_t ast = a_ring + sa.idx * kAUnitBytes + team * kABytes;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) sts128(ast + st_off[j], v[j][0], v[j][1], v[j][2], v[j][3]);
+          for (int jj = 0; jj < 4; ++jj) sts128(ast + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
+#pragma unroll
+          for (int ps = 1; ps < R::kRows; ++ps) {
+            decode_row<FMT>(wa[ps], wb[ps], sraw[ps], sf[ps], tscale, valid[ps], v);
+            const uint32_t ar = ast + ps * R::kRowStep * 128;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) sts128(ar + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
+          }
           // This CTA's grad_out half must have landed before the operand-ready arrival: the
           // even CTA's MMA thread only watches the arrivals.
           ok = wait_phase(smem_u32(&sh.b_full[sa.idx]), sa.par, abort_flag, p.err, limit);
@@ -674,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // not reach the products: zero them in both boxes of this CTA's half.
             const uint32_t b_tile = smem_u32(ring_b + sa.idx * kBUnitBytes + team * kBBytes);
             const int dt = dw * 32 + lane;
-            for (int idx = dt; idx < (kTileK - kvalid) * 8 * 2; idx += 256) {
+            for (int idx = dt; idx < (kTileK - kvalid) * 8 * 2; idx += 32 * R::kDeqPerTeam) {
               const int box = idx / ((kTileK - kvalid) * 8);
               const int rem = idx % ((kTileK - kvalid) * 8);
               const int rr = kvalid + rem / 8, c = rem % 8;
@@ -839,7 +898,15 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   const int64_t bound = OP == kDgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
   static_assert(F::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
-  auto kern = bsq_gemm_kernel<FMT, OP>;
+  // Kernel: the short-tile variant (more epilogue warps) for wgrad of a packed format whose
+  // experts average fewer than 1024 rows, i.e. tiles of at most 16 k-blocks where the
+  // epilogue sets the pace; BSQ_GEMM_SHORT_TILES=0/1 forces the choice.
+  auto kern = bsq_gemm_kernel<FMT, OP, false>;
+  if constexpr (OP == kWgrad && FMT != BSQ_BF16) {
+    const char* env = std::getenv("BSQ_GEMM_SHORT_TILES");
+    const bool shortk = env && env[0] ? env[0] == '1' : a.S < 1024 * a.E;
+    if (shortk) kern = bsq_gemm_kernel<FMT, OP, true>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   cudaLaunchConfig_t cfg = {};

@@ -47,6 +47,13 @@
  *     workspace per device (16*K*4 bytes plus counters, at least 1 MiB) that the first such
  *     call allocates and a later call with a larger K re-allocates; make the first small-M
  *     call before any stream capture.  bsq_linear_dgrad_smallm_noalloc allocates nothing.
+ *   - Environment (read by the host side; none changes a result beyond FP32 summation order):
+ *       BSQ_WAIT_LIMIT_MS     bound of every pipeline wait inside a kernel (default 2000);
+ *                             on expiry the kernel stops and records BSQ_DEVERR_TIMEOUT.
+ *       BSQ_GEMM_SHORT_TILES  GEMM kernel for wgrad of packed formats: unset = chosen per
+ *                             call (the short-tile kernel, with more epilogue warps, when
+ *                             the experts average fewer than 1024 rows), 0 = never, 1 = always.
+ *                             Read at every call.
  */
 #ifndef BSQ_H
 #define BSQ_H

@@ -45,9 +45,23 @@ def test_linear_dgrad(fmt, M, N, K):
     _no_device_error()
 
 
+# wgrad of a packed format has two kernels (default and short-tile); "auto" lets the
+# library choose, "0" / "1" force each one through BSQ_GEMM_SHORT_TILES.
+KERNELS = ["auto", "0", "1"]
+
+
+def _select_kernel(monkeypatch, kernel):
+    if kernel == "auto":
+        monkeypatch.delenv("BSQ_GEMM_SHORT_TILES", raising=False)
+    else:
+        monkeypatch.setenv("BSQ_GEMM_SHORT_TILES", kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("M,N,K", [(300, 200, 352), (100, 520, 256), (1, 64, 128), (64, 128, 256)])
-def test_linear_wgrad(fmt, M, N, K):
+@pytest.mark.parametrize("M,N,K", [(300, 200, 352), (100, 520, 256), (1, 64, 128), (64, 128, 256), (1100, 264, 640)])
+def test_linear_wgrad(fmt, M, N, K, kernel, monkeypatch):
+    _select_kernel(monkeypatch, kernel)
     X = synth.make_packed(fmt, 1, M, K, 1.0, seed=21 + fmt, device="cpu")
     G = _grad(M, N, 22)
     out = bsq.linear_wgrad(G.cuda(), X.to("cuda"))
@@ -143,9 +157,11 @@ def test_grouped_dgrad(fmt, ci):
     _no_device_error()
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ci", range(len(GROUPED_COUNTS)))
-def test_grouped_wgrad(fmt, ci):
+def test_grouped_wgrad(fmt, ci, kernel, monkeypatch):
+    _select_kernel(monkeypatch, kernel)
     counts = GROUPED_COUNTS[ci]
     S, N, K = sum(counts) + 9, 200, 352
     E = len(counts)
