@@ -898,14 +898,13 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   const int64_t bound = OP == kDgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
   static_assert(F::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
-  // Kernel: the short-tile variant (more epilogue warps) for wgrad of a packed format whose
-  // experts average fewer than 1024 rows, i.e. tiles of at most 16 k-blocks where the
-  // epilogue sets the pace; BSQ_GEMM_SHORT_TILES=0/1 forces the choice.
+  // Kernel: the short-tile variant (more epilogue warps) for wgrad of a packed format is
+  // opt-in (BSQ_GEMM_SHORT_TILES=1); it is meant for experts averaging fewer than 1024
+  // rows, where a tile has at most 16 k-blocks and the epilogue sets the pace.
   auto kern = bsq_gemm_kernel<FMT, OP, false>;
   if constexpr (OP == kWgrad && FMT != BSQ_BF16) {
     const char* env = std::getenv("BSQ_GEMM_SHORT_TILES");
-    const bool shortk = env && env[0] ? env[0] == '1' : a.S < 1024 * a.E;
-    if (shortk) kern = bsq_gemm_kernel<FMT, OP, true>;
+    if (env && env[0] == '1') kern = bsq_gemm_kernel<FMT, OP, true>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);

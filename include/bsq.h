@@ -50,10 +50,9 @@
  *   - Environment (read by the host side; none changes a result beyond FP32 summation order):
  *       BSQ_WAIT_LIMIT_MS     bound of every pipeline wait inside a kernel (default 2000);
  *                             on expiry the kernel stops and records BSQ_DEVERR_TIMEOUT.
- *       BSQ_GEMM_SHORT_TILES  GEMM kernel for wgrad of packed formats: unset = chosen per
- *                             call (the short-tile kernel, with more epilogue warps, when
- *                             the experts average fewer than 1024 rows), 0 = never, 1 = always.
- *                             Read at every call.
+ *       BSQ_GEMM_SHORT_TILES  1 = wgrad of packed formats runs the short-tile GEMM kernel
+ *                             (more epilogue warps; for experts averaging fewer than 1024
+ *                             rows); otherwise the default kernel.  Read at every call.
  */
 #ifndef BSQ_H
 #define BSQ_H

@@ -45,8 +45,8 @@ def test_linear_dgrad(fmt, M, N, K):
     _no_device_error()
 
 
-# wgrad of a packed format has two kernels (default and short-tile); "auto" lets the
-# library choose, "0" / "1" force each one through BSQ_GEMM_SHORT_TILES.
+# wgrad of a packed format has two kernels (default and short-tile, opt-in); "auto" leaves
+# BSQ_GEMM_SHORT_TILES unset, "0" / "1" set it.
 KERNELS = ["auto", "0", "1"]
 
 
