@@ -743,7 +743,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_rank(smem_u32(&sh.a_full[sa.idx]), 0);
+        if (lane == 0) {
+          // Zeroed grad_out rows are generic writes to the exchanged B operand, which the
+          // other SM's tensor core reads too: announce them with a cluster-scope release
+          // (one k-block per expert tile at most, so the cost stays off the main path).
+          if (OP == kWgrad && present && kvalid < kTileK) mbar_arrive_rank_cl(smem_u32(&sh.a_full[sa.idx]), 0);
+          else mbar_arrive_rank(smem_u32(&sh.a_full[sa.idx]), 0);
+        }
       }
       if (!ok) break;
       uc += units;

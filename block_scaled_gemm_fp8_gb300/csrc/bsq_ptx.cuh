@@ -94,6 +94,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_rank(uint32_t bar, uint32_t rank) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(bar, rank)) : "memory");
 }
+// As mbar_arrive_rank with a cluster-scope release: announces generic writes to this CTA's
+// part of the exchanged B operand of a pair MMA, which the other SM's tensor core reads.
+__device__ __forceinline__ void mbar_arrive_rank_cl(uint32_t bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(bar, rank))
+               : "memory");
+}
 // 32-bit store to the same offset in CTA `rank`.
 __device__ __forceinline__ void st_rank_u32(uint32_t addr, uint32_t rank, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_rank(addr, rank)), "r"(v) : "memory");
