@@ -21,7 +21,7 @@
 // bytes each SM stages halves the L2->SM traffic per FLOP and the shared memory needed to
 // keep the TMA round trip (over a microsecond) covered.
 //
-// Per CTA (one per SM), 24 warps:
+// Per CTA (one per SM), 24 warps (default kernel; see Roles for the short-tile one):
 //   warp 0      TMA producer of the packed ring: packed tiles and FP4 scale tiles
 //   warp 2      allocates / frees TMEM
 //   warp 3      TMA producer of the grad_out ring: this CTA's half of the unit's tiles
@@ -39,8 +39,11 @@
 // their "slot free" barrier, so the single MMA thread handles one wait, eight MMAs and
 // one commit per unit.  It waits on its own CTA's "operand ready" barrier only, which
 // every dequant warp of both CTAs arrives on once its A rows are written and its own
-// CTA's grad_out half has landed.  MMA completion is multicast to both CTAs' "slot
-// free" barriers.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
+// CTA's grad_out half has landed.  Those arrivals carry a CTA-scope release: the A rows
+// are read only by the arriving CTA's own tensor core, and the grad_out halves (read by
+// both SMs) are TMA-written and complete before the arrival; only grad_out rows zeroed
+// by ordinary stores (grouped wgrad) need, and get, a cluster-scope release.  MMA
+// completion is multicast to both CTAs' "slot free" barriers.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
 // overlap the main loop of the next.  Tiles are walked in a static persistent order;
 // each role finds a tile's expert with its own forward cursor over the offsets (read
 // through the read-only cache, so no table takes shared memory).  Every wait is
