@@ -408,6 +408,24 @@ def cpu_threads():
     return os.cpu_count()
 
 
+# ---------------------------------------------------------------- replicas
+def max_over_ranks(value, device=None):
+    """The largest value over the ranks of the initialised process group (the slowest
+    replica sets the job's time), or `value` itself when there is no group of two or more."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() < 2:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_step, steps, total_ms):
+    """Whole-job throughput: every replica does flops_per_step per step; the job takes total_ms."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- main
 def main():
     args = parse_args()
@@ -469,13 +487,8 @@ def main():
     per_op, step_ms, launches = time_ops(c, outs, bsq, args.steps, args.warmup, flush)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        total_ms = float(t.item())
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(sum(step_ms), device=dev)
+    value = job_tflops(world, flops_step, args.steps, total_ms)
     st, code = bsq.get_device_error()
     if st != 0:
         raise SystemExit(f"device error {code} during the benchmark")

@@ -82,3 +82,35 @@ def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.profiled_traffic("w", "dgrad") == 123
     assert bench.profiled_traffic("w", "wgrad") is None       # taken on other sources
     assert bench.profiled_traffic("other", "dgrad") is None   # no capture for the workload
+
+
+def _rank_main(rank, world, port, values, out):
+    import os
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        out[rank] = bench.max_over_ranks(values[rank])
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_take_the_slowest_rank():
+    # two gloo ranks on the CPU, as the N-GPU bench runs one replica per rank
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    values = [12.5, 40.0]
+    manager = mp.get_context("spawn").Manager()
+    out = manager.dict()
+    mp.start_processes(_rank_main, args=(2, port, values, out), nprocs=2, start_method="spawn", join=True)
+    assert dict(out) == {0: 40.0, 1: 40.0}
+
+
+def test_single_process_and_job_throughput():
+    assert bench.max_over_ranks(7.0) == 7.0           # no process group: unchanged
+    # 2 replicas x 1 TFLOP per step x 10 steps in 20 ms -> 1000 TFLOP/s for the job
+    assert bench.job_tflops(2, 1e12, 10, 20.0) == pytest.approx(1000.0)
