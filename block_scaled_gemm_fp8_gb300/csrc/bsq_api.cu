@@ -19,7 +19,7 @@ thread_local char g_msg[512] = "";
 // bsq_get_device_error.  One int per device, allocated with the module.
 __device__ int32_t g_device_error;
 
-constexpr int kMaxDevices = 64;
+using bsq::kMaxDevices;
 int32_t* g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
 // Per-device FP32 workspace of the split-K small-M dgrad (zero between calls; grown on demand).
@@ -166,12 +166,12 @@ int set_error(int status, const char* message) {
   return fail(static_cast<bsq_status>(status), "%s", message);
 }
 uint64_t wait_limit_ns() {
-  static uint64_t v = [] {
-    const char* s = std::getenv("BSQ_WAIT_LIMIT_MS");
-    const long ms = s ? std::atol(s) : 0;
-    return static_cast<uint64_t>(ms > 0 ? ms : 2000) * 1000000ull;
-  }();
-  return v;
+  const char* us = std::getenv("BSQ_WAIT_LIMIT_US");
+  const long u = us ? std::atol(us) : 0;
+  if (u > 0) return static_cast<uint64_t>(u) * 1000ull;
+  const char* ms = std::getenv("BSQ_WAIT_LIMIT_MS");
+  const long m = ms ? std::atol(ms) : 0;
+  return static_cast<uint64_t>(m > 0 ? m : 2000) * 1000000ull;
 }
 }  // namespace bsq
 

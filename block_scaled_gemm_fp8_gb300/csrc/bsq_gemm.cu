@@ -23,7 +23,7 @@
 //
 // Per CTA (one per SM), 24 warps (default kernel; see Roles for the short-tile one):
 //   warp 0      TMA producer of the packed ring: packed tiles and FP4 scale tiles
-//   warp 2      allocates / frees TMEM
+//   warp 2      allocates / frees TMEM; one lane relays "operand ready" to the even CTA
 //   warp 3      TMA producer of the grad_out ring: this CTA's half of the unit's tiles
 //   warp 1      MMA issuer, one thread of the even CTA: 4 x (256 x Nm x 16) per k-block
 //   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
@@ -37,20 +37,26 @@
 // of a ring is waited on by the same threads in unit order (a parity wait cannot then
 // mistake a phase two laps away for its own).  The operand and grad_out rings share
 // their "slot free" barrier, so the single MMA thread handles one wait, eight MMAs and
-// one commit per unit.  It waits on its own CTA's "operand ready" barrier only, which
-// every dequant warp of both CTAs arrives on once its A rows are written and its own
-// CTA's grad_out half has landed.  Those arrivals carry a CTA-scope release: the A rows
-// are read only by the arriving CTA's own tensor core, and the grad_out halves (read by
-// both SMs) are TMA-written and complete before the arrival; only grad_out rows zeroed
-// by ordinary stores (grouped wgrad) need, and get, a cluster-scope release.  MMA
-// completion is multicast to both CTAs' "slot free" barriers.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
+// one commit per unit.
+// Operand-ready protocol.  The pair MMA issued by the even CTA reads shared memory of
+// both CTAs, so what each CTA wrote for a unit must be released at cluster scope to the
+// issuing thread.  Every dequant warp arrives on its own CTA's a_local barrier once its
+// A rows (and any grad_out rows it zeroed) are written and fenced to the async proxy;
+// one relay thread per CTA waits for a_local and for the CTA's grad_out half (TMA bytes),
+// then arrives once on the even CTA's a_full with a cluster-scope release.  The MMA
+// thread acquires a_full at cluster scope.  One cluster release per unit per CTA keeps
+// the cost of the release off the dequant warps.  MMA completion is multicast to both
+// CTAs' "slot free" barriers; the odd CTA's epilogue releases TMEM with a cluster-scope
+// arrival too.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
 // overlap the main loop of the next.  Tiles are walked in a static persistent order;
 // each role finds a tile's expert with its own forward cursor over the offsets (read
 // through the read-only cache, so no table takes shared memory).  Every wait is
 // bounded by %globaltimer and records a timeout in the device error word (and stops the
 // peer CTA) instead of hanging.
-#include <cuda_bf16.h>
+#include <atomic>
 #include <cstdlib>
+
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "bsq_decode.cuh"
@@ -140,7 +146,8 @@ struct Params {
 struct SharedTail {
   uint64_t p_full[kMaxStages];    // per unit: the packed tiles landed (TMA bytes)
   uint64_t p_empty[kMaxStages];   // per unit: every dequant warp of this CTA has read its half
-  uint64_t a_full[kMaxStages];    // per unit: both CTAs' dequant warps (operand written, grad_out seen)
+  uint64_t a_local[kMaxStages];   // per unit: this CTA's dequant warps wrote their A rows
+  uint64_t a_full[kMaxStages];    // per unit (even CTA's is used): both CTAs' relays (operands in place)
   uint64_t op_empty[kMaxStages];  // per unit: the unit's MMAs completed (frees its A and B slots)
   uint64_t b_full[kMaxStages];    // per unit: this CTA's grad_out half landed (TMA bytes)
   uint64_t tmem_full[2];
@@ -344,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sh.p_empty[s]), R::kDeqPerTeam * kDeqTeams);   // every dequant warp of this CTA
     }
     for (int s = 0; s < kUStages; ++s) {
-      mbar_init(smem_u32(&sh.a_full[s]), R::kDeqPerTeam * kDeqTeams * kPair);   // every dequant warp of both CTAs (even CTA's is used)
+      mbar_init(smem_u32(&sh.a_local[s]), R::kDeqPerTeam * kDeqTeams);   // every dequant warp of this CTA
+      mbar_init(smem_u32(&sh.a_full[s]), kPair);                         // the relay of each CTA
       mbar_init(smem_u32(&sh.op_empty[s]), 1);
       mbar_init(smem_u32(&sh.b_full[s]), 1);
     }
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
-      if (*abort_flag) drain_pending<F::kPUnits>(sh.p_full, pend_mask, pend_par, limit);
+      if (*abort_flag) drain_pending<F::kPUnits>(sh.p_full, pend_mask, pend_par, kDrainLimitNs);
     }
   } else if (warp == 3) {
     // ===== TMA producer: this CTA's half of the grad_out ring, one unit at a time =====
@@ -477,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
-      if (*abort_flag) drain_pending<kUStages>(sh.b_full, pend_mask, pend_par, limit);
+      if (*abort_flag) drain_pending<kUStages>(sh.b_full, pend_mask, pend_par, kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ===== MMA issuer: one thread of the even CTA drives the pair =====
@@ -494,9 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            : sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B: MN-major
       constexpr uint32_t kBStep = OP == kDgrad ? (32 >> 4) : (2048 >> 4);   // 16 k of the B tile
       const uint32_t a_full0 = smem_u32(&sh.a_full[0]), op_empty0 = smem_u32(&sh.op_empty[0]);
-      // A unit is ready once every dequant warp of both CTAs has arrived: each arrives only
-      // after it has seen its own CTA's grad_out half land, so the grad_out halves need no
-      // wait of their own here.
+      // A unit is ready once both CTAs' relays have arrived: each has seen its CTA's A rows
+      // written and its grad_out half landed, and released them at cluster scope.
       auto ready = [&](uint32_t s, uint32_t q) { return wait_phase<true>(a_full0 + 8 * s, q, abort_flag, p.err, limit); };
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
         const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
@@ -539,6 +546,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++acc;
       }
     }
+  } else if (warp == 2) {
+    // ===== operand-ready relay: one thread per CTA =====
+    // Per unit: this CTA's dequant warps have written (and fenced) their A rows, and its
+    // grad_out half has landed; one arrival on the even CTA's a_full announces both, with
+    // a cluster-scope release because the other SM's tensor core reads them too.
+    if (lane == 0) {
+      uint32_t uc = 0;
+      ExpertCursor cur = cursor_begin<OP>(p);
+      const uint32_t a_full0 = smem_u32(&sh.a_full[0]);
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
+        const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
+        bool ok = true;
+        for (int j = 0; j < units; ++j, ++uc) {
+          const Slot sl = ring_slot<kUStages>(uc);
+          if (!wait_phase(smem_u32(&sh.a_local[sl.idx]), sl.par, abort_flag, p.err, limit) ||
+              !wait_phase(smem_u32(&sh.b_full[sl.idx]), sl.par, abort_flag, p.err, limit)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_rank_cl(a_full0 + 8 * sl.idx, 0);
+        }
+        if (!ok) break;
+      }
+    }
   } else if (warp >= 4 && warp < 4 + R::kEpiWarps) {
     // ===== epilogue =====
     // Warp w reads TMEM lane quarter w % 4; the kEpiPerQuarter warps of a quarter take its
@@ -573,21 +605,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int nchunks = (ti.n_valid + 31) >> 5;
-      if (sub >= nchunks) {
-        // no chunk for this warp: release the accumulator at once
+      // The even CTA's MMA thread reuses the accumulator once every epilogue warp of both
+      // CTAs has released it (the odd CTA's releases are cluster-scope).
+      auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_rank(smem_u32(&sh.tmem_empty[buf]), 0);
-      }
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(smem_u32(&sh.tmem_empty[buf]));
+          else mbar_arrive_rank_cl(smem_u32(&sh.tmem_empty[buf]), 0);
+        }
+      };
+      if (sub >= nchunks) release_acc();   // no chunk for this warp: release at once
       for (int c = sub; c < nchunks; c += R::kEpiPerQuarter) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + c * 32, v);
         tmem_wait_ld();
-        if (c + R::kEpiPerQuarter >= nchunks) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_rank(smem_u32(&sh.tmem_empty[buf]), 0);   // the even CTA's MMA reuses it
-        }
+        if (c + R::kEpiPerQuarter >= nchunks) release_acc();
         if (mok) {
           const int nlim = min(32, ti.n_valid - c * 32);
 #pragma unroll
@@ -726,14 +759,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) sts128(ar + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
           }
-          // This CTA's grad_out half must have landed before the operand-ready arrival: the
-          // even CTA's MMA thread only watches the arrivals.
-          ok = wait_phase(smem_u32(&sh.b_full[sa.idx]), sa.par, abort_flag, p.err, limit);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
           if (OP == kWgrad && kvalid < kTileK) {
             // grad_out rows past the expert (possibly uninitialised past offsets[E-1]) must
-            // not reach the products: zero them in both boxes of this CTA's half.
+            // not reach the products: once this CTA's grad_out half has landed, zero them in
+            // both boxes of the half.
+            ok = wait_phase(smem_u32(&sh.b_full[sa.idx]), sa.par, abort_flag, p.err, limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
             const uint32_t b_tile = smem_u32(ring_b + sa.idx * kBUnitBytes + team * kBBytes);
             const int dt = dw * 32 + lane;
             for (int idx = dt; idx < (kTileK - kvalid) * 8 * 2; idx += 32 * R::kDeqPerTeam) {
@@ -746,13 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) {
-          // Zeroed grad_out rows are generic writes to the exchanged B operand, which the
-          // other SM's tensor core reads too: announce them with a cluster-scope release
-          // (one k-block per expert tile at most, so the cost stays off the main path).
-          if (OP == kWgrad && present && kvalid < kTileK) mbar_arrive_rank_cl(smem_u32(&sh.a_full[sa.idx]), 0);
-          else mbar_arrive_rank(smem_u32(&sh.a_full[sa.idx]), 0);
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&sh.a_local[sa.idx]));   // this CTA's relay passes it on
       }
       if (!ok) break;
       uc += units;
@@ -766,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // once the drain barrier fires.
     umma_commit_pair(smem_u32(&sh.drain), 1);
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(smem_u32(&sh.drain), 0) && global_timer_ns() - t0 < limit) {
+    while (!mbar_try_wait(smem_u32(&sh.drain), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
     }
   }
   tc_fence_before();
@@ -907,13 +933,16 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   const int64_t bound = OP == kDgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
   static_assert(F::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
-  // Kernel: the short-tile variant (more epilogue warps) for wgrad of a packed format is
-  // opt-in (BSQ_GEMM_SHORT_TILES=1); it is meant for experts averaging fewer than 1024
-  // rows, where a tile has at most 16 k-blocks and the epilogue sets the pace.
+  // Kernel: wgrad of a packed format whose groups average fewer than 1024 rows (a tile of
+  // at most 16 k-blocks, where the epilogue sets the pace) takes the short-tile variant
+  // (more epilogue warps).  BSQ_GEMM_SHORT_TILES=1 / 0 forces one or the other.
   auto kern = bsq_gemm_kernel<FMT, OP, false>;
+  bool short_tiles = false;
   if constexpr (OP == kWgrad && FMT != BSQ_BF16) {
     const char* env = std::getenv("BSQ_GEMM_SHORT_TILES");
-    if (env && env[0] == '1') kern = bsq_gemm_kernel<FMT, OP, true>;
+    if (env && (env[0] == '0' || env[0] == '1')) short_tiles = env[0] == '1';
+    else short_tiles = a.S < 1024 * a.E;
+    if (short_tiles) kern = bsq_gemm_kernel<FMT, OP, true>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -929,13 +958,19 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // Persistent grid: as many pairs as can be resident at once (a GPC with an odd number of
-  // free SMs leaves one idle), never more than there are pair tiles.
-  static int max_clusters = 0;
+  // free SMs leaves one idle), never more than there are pair tiles.  The count is kept per
+  // kernel variant and device.
+  static std::atomic<int> max_clusters_of[2][kMaxDevices];
+  int dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
+  int max_clusters = e == cudaSuccess ? max_clusters_of[short_tiles][dev].load() : 0;
   if (e == cudaSuccess && max_clusters == 0) {
     cfg.gridDim = dim3(kPair * (a.num_sms / kPair));
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     max_clusters = n > 0 ? n : a.num_sms / kPair;
+    max_clusters_of[short_tiles][dev].store(max_clusters);
   }
   int64_t clusters = bound < max_clusters ? bound : max_clusters;
   if (clusters < 1) clusters = 1;

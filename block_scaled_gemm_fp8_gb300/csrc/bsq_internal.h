@@ -18,6 +18,7 @@ constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kTileK = 64;
 constexpr int kMaxExperts = 1024;
+constexpr int kMaxDevices = 64;   // device ordinals the per-device host state covers
 
 struct GemmArgs {
   int op;            // kDgrad / kWgrad
@@ -81,7 +82,12 @@ int device_error_word(int32_t** err, int* sms);
 // Record a message for bsq_last_error() and return `status`.
 int set_error(int status, const char* message);
 
-// Wait limit of every pipeline wait inside the kernels (nanoseconds of %globaltimer).
+// Wait limit of every pipeline wait inside the kernels (nanoseconds of %globaltimer),
+// read from the environment at every call: BSQ_WAIT_LIMIT_US, else BSQ_WAIT_LIMIT_MS,
+// else 2 s.
 uint64_t wait_limit_ns();
+// Limit of the waits an aborting kernel makes for its own copies and MMAs still in flight
+// (they complete in microseconds; the limit only guards against a copy that never does).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 }  // namespace bsq

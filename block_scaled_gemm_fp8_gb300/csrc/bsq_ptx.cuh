@@ -86,16 +86,10 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on the barrier at the same offset in CTA `rank`, with the default (CTA-scope)
-// release.  Used to announce data in the ARRIVING CTA's own shared memory that its own
-// SM's tensor core reads (after fence_proxy_async_smem), or TMEM reads that are done; a
-// cluster-scope release here costs ~0.7 us per arrival under load and is not needed for
-// that pattern.
-__device__ __forceinline__ void mbar_arrive_rank(uint32_t bar, uint32_t rank) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(bar, rank)) : "memory");
-}
-// As mbar_arrive_rank with a cluster-scope release: announces generic writes to this CTA's
-// part of the exchanged B operand of a pair MMA, which the other SM's tensor core reads.
+// Arrive on the barrier at the same offset in CTA `rank` of the cluster with a
+// cluster-scope release: everything the arriving thread has written or observed (for
+// example shared-memory operands that other threads wrote and announced to it) is
+// visible to a thread of that CTA that acquires the phase at cluster scope.
 __device__ __forceinline__ void mbar_arrive_rank_cl(uint32_t bar, uint32_t rank) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(bar, rank))
                : "memory");

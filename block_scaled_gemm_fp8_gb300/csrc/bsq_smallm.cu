@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
 #pragma unroll
   for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-  // bounded wait for the slab
+  // bounded wait for the slab; the CTA takes one decision (a thread that gave up stops all)
   bool ok = true;
   {
     const uint64_t t0 = global_timer_ns();
@@ -169,9 +169,8 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
       }
     }
   }
-  if (!ok) {
-    if (tid == 0) atomicCAS(p.err, 0, BSQ_DEVERR_TIMEOUT);
-  } else {
+  ok = __syncthreads_and(ok) != 0;
+  if (ok) {
     const int nsteps = (nrows + kStep - 1) / kStep;
     for (int ks = warp; ks < nsteps; ks += kWarps) {
       const int lr = ks * kStep;               // local row of this k-step
@@ -252,6 +251,32 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
         }
       }
     }
+  }
+  if (!ok) {
+    // Orderly abort: record the timeout, give the copies still in flight one more bounded
+    // wait to land (nothing reads or reuses the staged region), write nothing, and keep
+    // only the workspace bookkeeping: the last CTA of the slab re-zeroes the slab's
+    // workspace and counter so later calls start clean.  grad_X of this call is undefined.
+    if (tid == 0) {
+      atomicCAS(p.err, 0, BSQ_DEVERR_TIMEOUT);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_u32(bar), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+      }
+    }
+    __syncthreads();
+    if (gridDim.y == 1) return;
+    __threadfence();
+    if (tid == 0) *last_flag = (atomicAdd(p.counters + slab, 1) == static_cast<int>(gridDim.y) - 1);
+    __syncthreads();
+    if (!*last_flag) return;
+    __threadfence();
+    for (int i = tid; i < 16 * kSlab / 4; i += kThreadsSm) {
+      const int t = (4 * i) / kSlab, c = cb + (4 * i) % kSlab;
+      if (t < p.M && c < p.K) __stcg(reinterpret_cast<float4*>(p.ws + static_cast<int64_t>(t) * p.K + c),
+                                     make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    if (tid == 0) p.counters[slab] = 0;
+    return;
   }
   __syncthreads();   // everyone is done with the staged slabs; reuse them for the partials
 
@@ -424,7 +449,7 @@ constexpr int64_t kStaticMaxK = 16384;  // largest K the static scratch serves
 constexpr size_t kStaticScratchBytes = 16 * kStaticMaxK * 4 + 4096;
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevicesStatic = 64;
+constexpr int kMaxDevicesStatic = bsq::kMaxDevices;
 void* g_static_ptr[kMaxDevicesStatic] = {};
 int g_static_sms[kMaxDevicesStatic] = {};
 std::mutex g_static_mu;

@@ -174,16 +174,29 @@ def random_codes(fmt, batch, rows, cols, seed, device="cpu", scale_kind="random"
 
     scale_kind: "random" (moderate positive scales), "edge" (extreme scales:
     E8M0 bytes 0/1/126/127/128/254, tiny and huge float32 scale_inv, E4M3
-    subnormal block scales) or "nan" (a few NaN scales).
+    subnormal block scales), "nan" (a few NaN scales) or "finite" (scales whose
+    products with every code stay finite but are often not BF16 numbers or are
+    subnormal: E8M0 bytes up to 200, float32 scale_inv with full mantissas over a
+    wide exponent range, NVFP4 tensor scales from 1e-30 to 1e30; FP8 NaN codes are
+    replaced by 448 so that every decoded value is finite).
     """
     g = _gen(device, seed)
     nbytes = cols if fmt == FMT_FP8 else cols // 2
     data = torch.randint(0, 256, (batch, rows, nbytes), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+    if fmt == FMT_FP8 and scale_kind == "finite":
+        data = torch.where((data & 0x7F) == 0x7F, data - 1, data)   # S.1111.111 (NaN) -> S.1111.110 (448)
     ts = None
     if fmt == FMT_FP8:
         shape = (batch, -(-rows // 128), -(-cols // 128))
         s = torch.rand(shape, generator=g, device=device) + 0.5
-        if scale_kind == "edge":
+        if scale_kind == "finite":
+            # |code| <= 448 and scale < 2^117 keep every product below the BF16 maximum
+            mant = torch.rand(shape, generator=g, device=device) + 1.0
+            exps = torch.tensor([-137, -134, -131, -128, -125, -121, -60, -7, -3, 0, 5, 40, 100, 116],
+                                dtype=torch.float32, device=device)
+            ex = exps[torch.randint(0, exps.numel(), shape, generator=g, device=device)]
+            s = mant * torch.pow(2.0, ex)
+        elif scale_kind == "edge":
             pool = torch.tensor([2.0 ** -130, 1e-40, 3.0e-39, 1.0, 0.1, 2.0 ** 7, 2.0 ** 8, 300.0,
                                  3.0e38, 1.17e-38, 2.0 ** -126, 7.0e-3], device=device)
             s = pool[torch.randint(0, pool.numel(), shape, generator=g, device=device)]
@@ -192,7 +205,10 @@ def random_codes(fmt, batch, rows, cols, seed, device="cpu", scale_kind="random"
         scale = s.to(torch.float32)
     elif fmt == FMT_MXFP4:
         shape = (batch, rows, cols // 32)
-        if scale_kind == "edge":
+        if scale_kind == "finite":
+            pool = torch.tensor([0, 1, 2, 100, 127, 128, 129, 130, 150, 180, 200], device=device)
+            scale = pool[torch.randint(0, pool.numel(), shape, generator=g, device=device)].to(torch.uint8)
+        elif scale_kind == "edge":
             pool = torch.tensor([0, 1, 126, 127, 128, 129, 142, 143, 200, 254], device=device)
             scale = pool[torch.randint(0, pool.numel(), shape, generator=g, device=device)].to(torch.uint8)
         elif scale_kind == "nan":
@@ -202,7 +218,12 @@ def random_codes(fmt, batch, rows, cols, seed, device="cpu", scale_kind="random"
             scale = torch.randint(110, 140, shape, generator=g, device=device).to(torch.uint8)
     elif fmt == FMT_NVFP4:
         shape = (batch, rows, cols // 16)
-        if scale_kind == "edge":
+        if scale_kind == "finite":
+            scale = torch.randint(0, 0x7F, shape, generator=g, device=device).to(torch.uint8)   # finite E4M3
+            scale = scale | (torch.randint(0, 2, shape, generator=g, device=device).to(torch.uint8) << 7)
+            tsv = torch.tensor([1e-30, 2.0 ** -120, 0.3712, 1e30, 7.3e-5, 3.1], device=device)
+            ts = tsv[torch.arange(batch, device=device) % tsv.numel()].to(torch.float32)
+        elif scale_kind == "edge":
             scale = torch.randint(0, 256, shape, generator=g, device=device).to(torch.uint8)
             tsv = torch.tensor([1e-30, 2.0 ** -120, 1.0, 3.0e35][:batch] + [0.5] * max(0, batch - 4), device=device)
             ts = tsv[:batch].to(torch.float32)

@@ -47,12 +47,16 @@
  *     workspace per device (16*K*4 bytes plus counters, at least 1 MiB) that the first such
  *     call allocates and a later call with a larger K re-allocates; make the first small-M
  *     call before any stream capture.  bsq_linear_dgrad_smallm_noalloc allocates nothing.
- *   - Environment (read by the host side; none changes a result beyond FP32 summation order):
- *       BSQ_WAIT_LIMIT_MS     bound of every pipeline wait inside a kernel (default 2000);
- *                             on expiry the kernel stops and records BSQ_DEVERR_TIMEOUT.
- *       BSQ_GEMM_SHORT_TILES  1 = wgrad of packed formats runs the short-tile GEMM kernel
- *                             (more epilogue warps; for experts averaging fewer than 1024
- *                             rows); otherwise the default kernel.  Read at every call.
+ *   - Environment (read by the host side at every call; none changes a result beyond FP32
+ *     summation order):
+ *       BSQ_WAIT_LIMIT_US,    bound of every pipeline wait inside a kernel, in microseconds
+ *       BSQ_WAIT_LIMIT_MS     or milliseconds (the first one set wins; default 2000 ms); on
+ *                             expiry the kernel lets its own copies and MMAs in flight finish,
+ *                             writes nothing more, returns and records BSQ_DEVERR_TIMEOUT; the
+ *                             outputs of that call are then undefined.
+ *       BSQ_GEMM_SHORT_TILES  wgrad of a packed format: 1 = the short-tile GEMM kernel (more
+ *                             epilogue warps), 0 = the default kernel; unset = the short-tile
+ *                             kernel when the groups average fewer than 1024 rows (S < 1024*E).
  */
 #ifndef BSQ_H
 #define BSQ_H

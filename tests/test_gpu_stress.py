@@ -1,0 +1,51 @@
+"""Repeated full-size runs of the pair-MMA GEMM kernels: against the oracle and against
+themselves.
+
+The tensor-core work of the GEMM kernels runs on pairs of SMs, and one CTA's operands
+are read by an MMA the other CTA issues.  A fault in the protocol that hands operands
+from one CTA to the other shows as one CTA's 128 x 256 block of some tile being wrong in
+some runs, not in every run.  So each workload here runs once and is checked against the
+float64 oracle on four columns of every 128-column block (every m-tile of every CTA),
+then runs REPS more times into buffers refilled with NaN; every tile's accumulation order
+is fixed, so each repeat must equal the first run bit for bit over the whole output.
+
+Workloads: MXFP4 4096^3 dense dgrad and wgrad, and the 128-expert MXFP4 grouped dgrad
+and wgrad (Dirichlet(0.3) routing, empty experts; its wgrad takes the short-tile kernel).
+"""
+
+import pytest
+import torch
+
+from block_scaled_gemm_fp8_gb300 import bsq, synth
+from tests._util import block_cols, check_config_sampled, run_config
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+REPS = 20
+
+
+@pytest.fixture(scope="module", params=[2, 5])
+def cfg(request):
+    c = synth.make_config(request.param, device="cuda")
+    yield c
+    del c
+    torch.cuda.empty_cache()
+
+
+def test_repeats_match_oracle_and_first_run(cfg):
+    c = cfg
+    first = run_config(c)
+    check_config_sampled(c, first, block_cols(c["K"], 4, 7))
+    ref = {k: v.clone() for k, v in first.items()}
+    bad = []
+    for rep in range(REPS):
+        for v in first.values():
+            v.fill_(float("nan"))
+        run_config(c, first)
+        for k, v in first.items():
+            if not torch.equal(v.view(torch.int16), ref[k].view(torch.int16)):
+                diff = (v.view(torch.int16) != ref[k].view(torch.int16))
+                bad.append((rep, k, int(diff.sum().item())))
+    st, code = bsq.get_device_error()
+    assert st == bsq.BSQ_OK and code == 0, (st, code)
+    assert not bad, f"{c['name']}: repeats that differ from the first run (rep, op, elements): {bad}"
