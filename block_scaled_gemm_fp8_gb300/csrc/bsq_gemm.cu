@@ -39,15 +39,17 @@
 // their "slot free" barrier, so the single MMA thread handles one wait, eight MMAs and
 // one commit per unit.
 // Operand-ready protocol.  The pair MMA issued by the even CTA reads shared memory of
-// both CTAs, so what each CTA wrote for a unit must be released at cluster scope to the
-// issuing thread.  Every dequant warp arrives on its own CTA's a_local barrier once its
-// A rows (and any grad_out rows it zeroed) are written and fenced to the async proxy;
-// one relay thread per CTA waits for a_local and for the CTA's grad_out half (TMA bytes),
-// then arrives once on the even CTA's a_full with a cluster-scope release.  The MMA
-// thread acquires a_full at cluster scope.  One cluster release per unit per CTA keeps
-// the cost of the release off the dequant warps.  MMA completion is multicast to both
-// CTAs' "slot free" barriers; the odd CTA's epilogue releases TMEM with a cluster-scope
-// arrival too.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
+// both CTAs, so what the odd CTA wrote for a unit must be released at cluster scope to
+// the issuing thread.  Every dequant warp arrives on its own CTA's a_local barrier once
+// its A rows (and any grad_out rows it zeroed) are written and fenced to the async
+// proxy; one relay thread per CTA waits for a_local and for the CTA's grad_out half (TMA
+// bytes).  The even relay then arrives on a_full expecting 4 transaction bytes; the odd
+// relay supplies them with an st.async into the even CTA whose complete-tx is a release
+// at cluster scope.  The MMA thread acquires a_full at cluster scope.  (An
+// mbarrier.arrive.release.cluster there stalls the SM and costs about 30 % of the
+// throughput; the st.async costs next to nothing.)  MMA completion is multicast to both
+// CTAs' "slot free" barriers; the odd CTA's epilogue hands TMEM back the same way as the
+// odd relay.  Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
 // overlap the main loop of the next.  Tiles are walked in a static persistent order;
 // each role finds a tile's expert with its own forward cursor over the offsets (read
 // through the read-only cache, so no table takes shared memory).  Every wait is
@@ -147,13 +149,14 @@ struct SharedTail {
   uint64_t p_full[kMaxStages];    // per unit: the packed tiles landed (TMA bytes)
   uint64_t p_empty[kMaxStages];   // per unit: every dequant warp of this CTA has read its half
   uint64_t a_local[kMaxStages];   // per unit: this CTA's dequant warps wrote their A rows
-  uint64_t a_full[kMaxStages];    // per unit (even CTA's is used): both CTAs' relays (operands in place)
+  uint64_t a_full[kMaxStages];    // per unit (even CTA's is used): even relay + 4 bytes from the odd relay
   uint64_t op_empty[kMaxStages];  // per unit: the unit's MMAs completed (frees its A and B slots)
   uint64_t b_full[kMaxStages];    // per unit: this CTA's grad_out half landed (TMA bytes)
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
+  uint32_t sink;                  // target of the odd CTA's st.async announcements (never read)
   uint32_t abort_flag;
   int32_t total_tiles;
   int32_t pad;
@@ -352,13 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kUStages; ++s) {
       mbar_init(smem_u32(&sh.a_local[s]), R::kDeqPerTeam * kDeqTeams);   // every dequant warp of this CTA
-      mbar_init(smem_u32(&sh.a_full[s]), kPair);                         // the relay of each CTA
+      mbar_init(smem_u32(&sh.a_full[s]), 1);                             // even relay; odd relay: tx bytes
       mbar_init(smem_u32(&sh.op_empty[s]), 1);
       mbar_init(smem_u32(&sh.b_full[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sh.tmem_full[b]), 1);
-      mbar_init(smem_u32(&sh.tmem_empty[b]), R::kEpiWarps * kPair);   // epilogue warps of both CTAs
+      mbar_init(smem_u32(&sh.tmem_empty[b]), R::kEpiWarps);   // even epilogue warps; odd ones: tx bytes
     }
     mbar_init(smem_u32(&sh.drain), 1);
     sh.abort_flag = 0u;
@@ -402,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t limit = p.timeout_ns;
   const int rank = static_cast<int>(cluster_ctarank());
   const int cl_id = blockIdx.x / kPair, n_cl = gridDim.x / kPair;
+  uint32_t mma_acc_uses = 0;   // MMA thread: tiles accumulated (accumulator buffer b: uses of b)
 
   // ---------------------------------------------------------------- roles
   if (warp == 0) {
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && rank == 0) {
       uint32_t iu = 0, pu = 0;   // ring slot and phase parity of the next unit
       ExpertCursor cur = cursor_begin<OP>(p);
-      uint32_t acc = 0;
+      uint32_t& acc = mma_acc_uses;
       const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), kBoxBytes, 1024);   // A: MN-major, atoms of 64 m at 8 KB
       const uint64_t bdesc0 = OP == kDgrad ? sdesc_sw128(smem_u32(ring_b), 16, 1024)          // B: K-major rows
                                            : sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B: MN-major
@@ -549,8 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2) {
     // ===== operand-ready relay: one thread per CTA =====
     // Per unit: this CTA's dequant warps have written (and fenced) their A rows, and its
-    // grad_out half has landed; one arrival on the even CTA's a_full announces both, with
-    // a cluster-scope release because the other SM's tensor core reads them too.
+    // grad_out half has landed.  The even relay arrives on a_full expecting 4 bytes; the
+    // odd relay's st.async delivers them with a cluster-scope release, because the even
+    // CTA's MMA thread issues the MMA that reads the odd CTA's operands.
     if (lane == 0) {
       uint32_t uc = 0;
       ExpertCursor cur = cursor_begin<OP>(p);
@@ -566,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_rank_cl(a_full0 + 8 * sl.idx, 0);
+          if (rank == 0) mbar_arrive_expect_tx(a_full0 + 8 * sl.idx, 4);
+          else st_async_tx_rank(smem_u32(&sh.sink), a_full0 + 8 * sl.idx, 0);
         }
         if (!ok) break;
       }
@@ -606,13 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int nchunks = (ti.n_valid + 31) >> 5;
       // The even CTA's MMA thread reuses the accumulator once every epilogue warp of both
-      // CTAs has released it (the odd CTA's releases are cluster-scope).
+      // CTAs has released it: an even warp arrives expecting 4 bytes, an odd warp delivers
+      // 4 bytes with an st.async (a cluster-scope release).
       auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (rank == 0) mbar_arrive(smem_u32(&sh.tmem_empty[buf]));
-          else mbar_arrive_rank_cl(smem_u32(&sh.tmem_empty[buf]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&sh.tmem_empty[buf]), 4);
+          else st_async_tx_rank(smem_u32(&sh.sink), smem_u32(&sh.tmem_empty[buf]), 0);
         }
       };
       if (sub >= nchunks) release_acc();   // no chunk for this warp: release at once
@@ -791,8 +798,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every MMA this thread issued has completed (and read the odd CTA's shared memory)
     // once the drain barrier fires.
     umma_commit_pair(smem_u32(&sh.drain), 1);
-    const uint64_t t0 = global_timer_ns();
+    uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(smem_u32(&sh.drain), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+    }
+    // The odd CTA's st.async releases of the last accumulators are never waited on by the
+    // main loop; they must land before this CTA's shared memory goes away.
+    if (!*abort_flag) {
+      for (uint32_t b = 0; b < 2; ++b) {
+        const uint32_t uses = (mma_acc_uses + 1u - b) / 2u;
+        if (uses == 0) continue;
+        t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&sh.tmem_empty[b]), (uses - 1u) & 1u) &&
+               global_timer_ns() - t0 < kDrainLimitNs) {
+        }
+      }
+    }
+  }
+  if (rank == 0 && *abort_flag) {
+    // After an abort the odd CTA may still have st.async announcements in flight to this
+    // CTA, which nothing waits for: give them time to land before the shared memory goes.
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < kAbortSettleNs) {
     }
   }
   tc_fence_before();

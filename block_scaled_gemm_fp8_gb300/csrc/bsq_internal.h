@@ -89,5 +89,7 @@ uint64_t wait_limit_ns();
 // Limit of the waits an aborting kernel makes for its own copies and MMAs still in flight
 // (they complete in microseconds; the limit only guards against a copy that never does).
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
+// Time an aborting CTA pair leaves for asynchronous stores between its CTAs to land.
+constexpr uint64_t kAbortSettleNs = 50000ull;
 
 }  // namespace bsq

@@ -86,12 +86,15 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on the barrier at the same offset in CTA `rank` of the cluster with a
-// cluster-scope release: everything the arriving thread has written or observed (for
-// example shared-memory operands that other threads wrote and announced to it) is
-// visible to a thread of that CTA that acquires the phase at cluster scope.
-__device__ __forceinline__ void mbar_arrive_rank_cl(uint32_t bar, uint32_t rank) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(bar, rank))
+// Asynchronous 4-byte store into CTA `rank`'s shared memory at `dst` (the same offset
+// there) that completes 4 transaction bytes on that CTA's barrier at `bar`.  The
+// complete-tx of st.async is a release at cluster scope (PTX memory consistency model):
+// a thread of that CTA that acquires the barrier's phase at cluster scope sees everything
+// the storing thread wrote or had observed before the store.  Unlike an
+// mbarrier.arrive.release.cluster, it does not stall the SM's memory pipeline.
+__device__ __forceinline__ void st_async_tx_rank(uint32_t dst, uint32_t bar, uint32_t rank) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(map_to_rank(dst, rank)),
+               "r"(0u), "r"(map_to_rank(bar, rank))
                : "memory");
 }
 // 32-bit store to the same offset in CTA `rank`.
