@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the headline workload (not the other four, nor the standalone dequant)")
     return ap.parse_args()
 
 
@@ -62,6 +64,16 @@ def packed_bytes(p):
     elif p.fmt == 3:
         b += n / 16 + 4 * p.batch
     return b
+
+
+def step_plan(c):
+    """(name, flops, algorithmic bytes) of the step's dominant launch when the step is one
+    fused backward launch (grad_out read once for both products), else None."""
+    if c["grouped"] or c["W"].fmt != c["X"].fmt:
+        return None
+    M, N, K = c["M"], c["N"], c["K"]
+    return ("backward", 4.0 * M * N * K,
+            packed_bytes(c["W"]) + packed_bytes(c["X"]) + 2 * M * N + 2 * M * K + 2 * N * K)
 
 
 def plan(c):
@@ -92,9 +104,23 @@ def peaks():
             return None
         hbm = find(["hbm_gbs", "hbm_GBps"])
         bf16 = find(["bf16_tflops", "bf16_TFLOPs"])
+        sus = find(["bf16_tflops_sustained"])
         if hbm and bf16:
-            return {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+            return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": sus or bf16, "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def op_roofline(flops, nbytes, ms, pk):
+    """Roofline of one launch: the binding resource at the measured peaks, what was achieved
+    against it (burst peak: each launch is timed on its own) and the sustained-peak fraction."""
+    t = ms * 1e-3
+    if flops / (pk["bf16_tflops"] * 1e12) >= nbytes / (pk["hbm_gbs"] * 1e9):
+        a = flops / t / 1e12
+        return {"bound": "tensor", "achieved": a, "unit": "TFLOP/s", "frac": a / pk["bf16_tflops"],
+                "frac_sustained": a / pk["bf16_tflops_sustained"]}
+    a = nbytes / t / 1e9
+    return {"bound": "hbm", "achieved": a, "unit": "GB/s", "frac": a / pk["hbm_gbs"],
+            "tflops": flops / t / 1e12}
 
 
 # The GEMM kernel's sources: a traffic figure captured from an earlier build is reported
@@ -178,12 +204,16 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- native arm
+def fused(c):
+    """A linear workload whose W and X share a format runs as one bsq_linear_backward launch."""
+    return not c["grouped"] and c["W"].fmt == c["X"].fmt
+
+
 def run_ops(c, ops_out, bsq, stream=None):
-    """Launch one step; returns the number of library kernels launched."""
+    """Launch one step (the backward of the layer); returns the number of library kernels launched."""
     if not c["grouped"]:
-        bsq.linear_dgrad(c["G"], c["W"], out=ops_out["dgrad"], stream=stream)
-        bsq.linear_wgrad(c["G"], c["X"], out=ops_out["wgrad"], stream=stream)
-        return 2
+        bsq.linear_backward(c["G"], c["W"], c["X"], grad_x=ops_out["dgrad"], grad_w=ops_out["wgrad"], stream=stream)
+        return 1 if fused(c) else 2
     bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=ops_out["grouped_dgrad"], stream=stream)
     n = 1
     if c["X"] is not None:
@@ -209,8 +239,27 @@ def alloc_outputs(c, dev):
 HOST_COVER_CYCLES = 400000
 
 
+def time_step(c, outs, bsq, steps, flush):
+    """CUDA-event time (ms) of each of `steps` L2-flushed steps, each one run_ops call."""
+    stream = torch.cuda.current_stream()
+    ts, launches = [], 0
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launches += run_ops(c, outs, bsq)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return ts, launches
+
+
 def time_ops(c, outs, bsq, steps, warmup, flush):
-    """Per-op CUDA-event times (ms) over `steps` L2-flushed steps, plus launches."""
+    """Per-op CUDA-event times (ms) over `steps` L2-flushed steps, each op through its own
+    single-product entry point, and the step times: those of the fused backward launch
+    where the workload has one, else the sum of the ops.  Returns (per_op, step_ms, launches
+    inside the timed steps)."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         run_ops(c, outs, bsq)
@@ -219,6 +268,8 @@ def time_ops(c, outs, bsq, steps, warmup, flush):
     per_op = {n: [] for n in names}
     step_ms = []
     launches = 0
+    if fused(c):
+        step_ms, launches = time_step(c, outs, bsq, steps, flush)
     for _ in range(steps):
         flush.zero_()
         torch.cuda._sleep(HOST_COVER_CYCLES)
@@ -232,12 +283,14 @@ def time_ops(c, outs, bsq, steps, warmup, flush):
                 bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=outs[n])
             else:
                 bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=outs[n])
-            launches += 1
+            if not fused(c):
+                launches += 1
             evs[i + 1].record(stream)
         torch.cuda.synchronize()
         for i, n in enumerate(names):
             per_op[n].append(evs[i].elapsed_time(evs[i + 1]))
-        step_ms.append(evs[0].elapsed_time(evs[-1]))
+        if not fused(c):
+            step_ms.append(evs[0].elapsed_time(evs[-1]))
     return per_op, step_ms, launches
 
 
@@ -350,6 +403,65 @@ def time_e2e(c, outs, bsq, steps, warmup):
     b.record(s_out)                           # after the last step's read-back
     torch.cuda.synchronize()
     return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
+    """Every op of workload n on freshly generated inputs: median ms, TFLOP/s and roofline
+    per op, and the step's TFLOP/s with its fractions of the burst and sustained peaks."""
+    c = synth.make_config(n, device=dev, seed=0)
+    if c["grouped"]:
+        c["offsets_dev"] = torch.from_numpy(c["offsets"]).to(dev)
+    outs = alloc_outputs(c, dev)
+    ops = plan(c)
+    per_op, step_ms, launches = time_ops(c, outs, bsq, steps, warmup, flush)
+    st, code = bsq.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error {code} during workload {n}")
+    r = {"ops": {}, "launches": launches}
+    for name, fl, nb in ops:
+        ms = statistics.median(per_op[name])
+        r["ops"][name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "roofline": op_roofline(fl, nb, ms, pk)}
+    ms = statistics.median(step_ms)
+    fl = sum(o[1] for o in ops)
+    r["step_ms"] = ms
+    r["tflops"] = fl / (ms * 1e-3) / 1e12
+    r["frac_burst"] = r["tflops"] / pk["bf16_tflops"]
+    r["frac_sustained"] = r["tflops"] / pk["bf16_tflops_sustained"]
+    deq = None
+    if n in DEQUANT_WORKLOADS:
+        deq = measure_dequant(c["W"], bsq, steps, warmup, flush, pk)
+    del c, outs
+    torch.cuda.empty_cache()
+    return r, deq
+
+
+# The standalone dequant is timed on the packed weight of these workloads (one per format).
+DEQUANT_WORKLOADS = (3, 4, 5)
+
+
+def measure_dequant(p, bsq, steps, warmup, flush, pk):
+    """bsq_dequant of a packed operand to BF16 in HBM: GB/s of algorithmic bytes (packed
+    bytes and scales read once, 2 bytes per element written)."""
+    out = torch.empty((p.batch, p.rows, p.cols), dtype=torch.bfloat16, device=p.data.device)
+    for _ in range(warmup):
+        bsq.dequant(p, out=out)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bsq.dequant(p, out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    nbytes = packed_bytes(p) + 2.0 * p.batch * p.rows * p.cols
+    del out
+    return {"shape": [p.batch, p.rows, p.cols], "fmt": p.fmt, "ms": ms, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
 
 
 # ---------------------------------------------------------------- the oracle as a baseline
@@ -494,20 +606,24 @@ def main():
         raise SystemExit(f"device error {code} during the benchmark")
 
     pk = peaks()
-    # dominant kernel: the op with the largest share of the step
-    avg = {n: statistics.mean(v) for n, v in per_op.items()}
-    dom = max(avg, key=avg.get)
-    dom_flops, dom_bytes = [(o[1], o[2]) for o in ops if o[0] == dom][0]
-    t_dom = avg[dom] * 1e-3
-    tensor_t = dom_flops / (pk["bf16_tflops"] * 1e12)
-    hbm_t = dom_bytes / (pk["hbm_gbs"] * 1e9)
-    if tensor_t >= hbm_t:
-        roof = {"bound": "tensor", "achieved": dom_flops / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    # dominant kernel: the fused backward launch where the step is one, else the op with
+    # the largest share of the step
+    sp = step_plan(c)
+    if sp is not None:
+        dom, dom_flops, dom_bytes = sp
+        dom_ms = statistics.mean(step_ms)
     else:
-        roof = {"bound": "hbm", "achieved": dom_bytes / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+        avg = {n: statistics.mean(v) for n, v in per_op.items()}
+        dom = max(avg, key=avg.get)
+        dom_flops, dom_bytes = [(o[1], o[2]) for o in ops if o[0] == dom][0]
+        dom_ms = avg[dom]
+    r = op_roofline(dom_flops, dom_bytes, dom_ms, pk)
+    roof = {"bound": r["bound"], "achieved": r["achieved"],
+            "peak": pk["bf16_tflops"] if r["bound"] == "tensor" else pk["hbm_gbs"], "unit": r["unit"],
+            "frac": r["frac"]}
     roof["traffic"] = profiled_traffic(c["name"], dom)
-    roof["kernel"] = f"bsq_gemm_kernel ({dom})"
+    roof["kernel"] = f"bsq_gemm_kernel ({'dgrad+wgrad, one launch' if dom == 'backward' else dom})"
+    roof["ms"] = dom_ms
     roof["peak_source"] = pk["source"]
 
     line = {"metric": "dgrad+wgrad TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -530,6 +646,21 @@ def main():
         ms, h2d, d2h = time_e2e(c, outs, bsq, max(3, args.steps // 2), 2)
         line["e2e"] = {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+    if not args.no_extra:
+        # the other workloads (parity-test shapes too) and the standalone dequant, each
+        # timed the same way; the headline line above is unchanged by them
+        extra, deq = {}, {}
+        for n in (1, 2, 3, 4, 5):
+            if n == args.config:
+                continue
+            r, d = measure_workload(n, bsq, synth, dev, max(5, args.steps // 2), args.warmup, flush, pk)
+            extra[synth.CONFIG_NAMES[n]] = r
+            if d is not None:
+                deq[synth.CONFIG_NAMES[n]] = d
+            line["gpu_launches_extra"] = line.get("gpu_launches_extra", 0) + r["launches"]
+        line["other_workloads"] = extra
+        line["dequant"] = deq
+        line["peaks"] = pk
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host_copies(c)
         ncols = 4096   # every output column of the MXFP4 4096^3 workload: the whole step, a few seconds

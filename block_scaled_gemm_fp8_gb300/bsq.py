@@ -19,6 +19,7 @@ HEADER_PATH = os.path.join(HERE, "..", "include", "bsq.h")
 
 BSQ_BF16, BSQ_FP8_E4M3_B128, BSQ_MXFP4, BSQ_NVFP4 = 0, 1, 2, 3
 BSQ_OK, BSQ_ERR_INVALID_ARG, BSQ_ERR_UNSUPPORTED, BSQ_ERR_CUDA, BSQ_ERR_TIMEOUT = 0, 1, 2, 3, 4
+BSQ_NEEDS_GRAD_X, BSQ_NEEDS_GRAD_W = 1, 2
 
 _c_void_p, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
 
@@ -30,6 +31,8 @@ SIGNATURES = {
                           _c_void_p, _c_void_p],
     "bsq_grouped_wgrad": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64,
                           _c_void_p, _c_void_p],
+    "bsq_linear_backward": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p,
+                            _c_void_p, _c_void_p, _i64, ctypes.c_uint32, _c_void_p, _c_void_p, _c_void_p],
     "bsq_linear_dgrad_smallm_noalloc": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64,
                                         _c_void_p, _c_void_p],
     "bsq_status_string": [_i32],
@@ -143,6 +146,25 @@ def linear_wgrad(grad_out, x, out=None, stream=None):
     _check(lib().bsq_linear_wgrad(_ptr(grad_out), M, N, x.fmt, _ptr(x.data), _ptr(x.scale), _ptr(x.tensor_scale),
                                   x.cols, _ptr(out), _stream(stream)))
     return out
+
+
+def linear_backward(grad_out, w, x, needs=BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD_W, grad_x=None, grad_w=None,
+                    stream=None):
+    """(grad_x, grad_w): grad_out @ deq(W) and grad_out^T @ deq(X), each only when `needs` asks
+    for it (None otherwise); one launch when both are wanted and W and X share a format."""
+    M, N = grad_out.shape
+    K = (w if w is not None else x).cols
+    if needs & BSQ_NEEDS_GRAD_X and grad_x is None:
+        grad_x = torch.empty((M, K), dtype=torch.bfloat16, device=grad_out.device)
+    if needs & BSQ_NEEDS_GRAD_W and grad_w is None:
+        grad_w = torch.empty((N, K), dtype=torch.bfloat16, device=grad_out.device)
+    f = lambda p, a: None if p is None else getattr(p, a)
+    _check(lib().bsq_linear_backward(
+        _ptr(grad_out), M, N, f(w, "fmt") or 0, _ptr(f(w, "data")), _ptr(f(w, "scale")), _ptr(f(w, "tensor_scale")),
+        f(x, "fmt") or 0, _ptr(f(x, "data")), _ptr(f(x, "scale")), _ptr(f(x, "tensor_scale")), K, needs,
+        _ptr(grad_x) if needs & BSQ_NEEDS_GRAD_X else None, _ptr(grad_w) if needs & BSQ_NEEDS_GRAD_W else None,
+        _stream(stream)))
+    return (grad_x if needs & BSQ_NEEDS_GRAD_X else None), (grad_w if needs & BSQ_NEEDS_GRAD_W else None)
 
 
 def grouped_dgrad(grad_out, w, offsets, out=None, stream=None):

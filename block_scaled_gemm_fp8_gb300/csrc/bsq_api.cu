@@ -120,16 +120,17 @@ bsq_status check_packed(const char* what, int32_t fmt, const void* data, const v
   return BSQ_OK;
 }
 
+// out_elems: elements of the output; an empty output may be null.
 bsq_status check_gemm_common(const char* what, const void* g, int64_t S, int64_t N, int32_t fmt, int64_t K,
-                             const void* out) {
+                             const void* out, int64_t out_elems) {
   if (S < 0 || N < 0 || K < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
   if (S > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(BSQ_ERR_UNSUPPORTED, "%s: size above 2^31-1", what);
   if (S * N > 0 && (!g || !aligned16(g))) return fail(BSQ_ERR_INVALID_ARG, "%s: grad_out null or not 16-byte aligned", what);
   if (N % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: N %% 8 != 0 (grad_out row pitch must be 16 bytes)", what);
   if (fmt == BSQ_NVFP4 && K % 32)
     return fail(BSQ_ERR_UNSUPPORTED, "%s: NVFP4 K %% 32 != 0 (packed row pitch must be 16 bytes)", what);
-  if (!out) return fail(BSQ_ERR_INVALID_ARG, "%s: null output", what);
-  if (!aligned16(out)) return fail(BSQ_ERR_INVALID_ARG, "%s: output not 16-byte aligned", what);
+  if (out_elems > 0 && !out) return fail(BSQ_ERR_INVALID_ARG, "%s: null output", what);
+  if (out_elems > 0 && !aligned16(out)) return fail(BSQ_ERR_INVALID_ARG, "%s: output not 16-byte aligned", what);
   return BSQ_OK;
 }
 
@@ -157,7 +158,7 @@ bsq_status zero_output(void* out, int64_t bytes, cudaStream_t s, const char* wha
 namespace bsq {
 int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
                             const void* w_scale, const float* w_tensor_scale, int64_t K, const void* grad_x) {
-  bsq_status st = check_gemm_common("bsq_linear_dgrad", grad_out, M, N, w_fmt, K, grad_x);
+  bsq_status st = check_gemm_common("bsq_linear_dgrad", grad_out, M, N, w_fmt, K, grad_x, M * K);
   if (st != BSQ_OK) return st;
   return check_packed("bsq_linear_dgrad", w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, true);
 }
@@ -238,7 +239,7 @@ bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N, int32_t 
                             const void* w_scale, const float* w_tensor_scale, int64_t K, void* grad_x,
                             void* stream) {
   const char* what = "bsq_linear_dgrad";
-  bsq_status st = check_gemm_common(what, grad_out, M, N, w_fmt, K, grad_x);
+  bsq_status st = check_gemm_common(what, grad_out, M, N, w_fmt, K, grad_x, M * K);
   if (st != BSQ_OK) return st;
   st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, true);
   if (st != BSQ_OK) return st;
@@ -270,7 +271,7 @@ bsq_status bsq_linear_wgrad(const void* grad_out, int64_t M, int64_t N, int32_t 
                             const void* x_scale, const float* x_tensor_scale, int64_t K, void* grad_w,
                             void* stream) {
   const char* what = "bsq_linear_wgrad";
-  bsq_status st = check_gemm_common(what, grad_out, M, N, x_fmt, K, grad_w);
+  bsq_status st = check_gemm_common(what, grad_out, M, N, x_fmt, K, grad_w, N * K);
   if (st != BSQ_OK) return st;
   st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, true);
   if (st != BSQ_OK) return st;
@@ -283,11 +284,56 @@ bsq_status bsq_linear_wgrad(const void* grad_out, int64_t M, int64_t N, int32_t 
   return run_gemm(a, what);
 }
 
+bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
+                               const void* w_scale, const float* w_tensor_scale, int32_t x_fmt, const void* x_data,
+                               const void* x_scale, const float* x_tensor_scale, int64_t K, uint32_t needs,
+                               void* grad_x, void* grad_w, void* stream) {
+  const char* what = "bsq_linear_backward";
+  if (needs & ~static_cast<uint32_t>(BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD_W))
+    return fail(BSQ_ERR_INVALID_ARG, "%s: unknown bits in needs (0x%x)", what, needs);
+  const bool want_x = (needs & BSQ_NEEDS_GRAD_X) != 0, want_w = (needs & BSQ_NEEDS_GRAD_W) != 0;
+  if (!want_x && !want_w) return BSQ_OK;
+  if (!want_w)
+    return bsq_linear_dgrad(grad_out, M, N, w_fmt, w_data, w_scale, w_tensor_scale, K, grad_x, stream);
+  if (!want_x)
+    return bsq_linear_wgrad(grad_out, M, N, x_fmt, x_data, x_scale, x_tensor_scale, K, grad_w, stream);
+  bsq_status st = check_gemm_common(what, grad_out, M, N, w_fmt, K, grad_x, M * K);
+  if (st != BSQ_OK) return st;
+  st = check_gemm_common(what, grad_out, M, N, x_fmt, K, grad_w, N * K);
+  if (st != BSQ_OK) return st;
+  st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, true);
+  if (st != BSQ_OK) return st;
+  st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, true);
+  if (st != BSQ_OK) return st;
+  // One launch for both products needs one packed format and enough token rows for the
+  // tensor-core dgrad (fewer go to the small-M kernel); otherwise the two entry points run
+  // one after the other on the stream.
+  if (w_fmt != x_fmt || M <= bsq::kSmallM || N == 0 || K == 0 || M == 0) {
+    st = bsq_linear_dgrad(grad_out, M, N, w_fmt, w_data, w_scale, w_tensor_scale, K, grad_x, stream);
+    if (st != BSQ_OK) return st;
+    return bsq_linear_wgrad(grad_out, M, N, x_fmt, x_data, x_scale, x_tensor_scale, K, grad_w, stream);
+  }
+  int32_t* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  bsq::GemmArgs d{};
+  d.op = bsq::kDgrad; d.fmt = w_fmt; d.p_data = w_data; d.p_scale = w_scale; d.p_tensor_scale = w_tensor_scale;
+  d.p_batch = 1; d.p_rows = N; d.kc = K; d.g = grad_out; d.S = M; d.N = N; d.offsets = nullptr; d.E = 1;
+  d.out = grad_x; d.stream = static_cast<cudaStream_t>(stream); d.err = err; d.num_sms = sms;
+  bsq::GemmArgs w = d;
+  w.op = bsq::kWgrad; w.p_data = x_data; w.p_scale = x_scale; w.p_tensor_scale = x_tensor_scale; w.p_rows = M;
+  w.out = grad_w;
+  const char* msg = "";
+  if (bsq::launch_gemm_backward(d, w, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
+  return BSQ_OK;
+}
+
 bsq_status bsq_grouped_dgrad(const void* grad_out, int64_t S, int64_t N, int32_t w_fmt, const void* w_data,
                              const void* w_scale, const float* w_tensor_scale, int64_t E, int64_t K,
                              const int32_t* offsets, void* grad_x, void* stream) {
   const char* what = "bsq_grouped_dgrad";
-  bsq_status st = check_gemm_common(what, grad_out, S, N, w_fmt, K, grad_x);
+  bsq_status st = check_gemm_common(what, grad_out, S, N, w_fmt, K, grad_x, S * K);
   if (st != BSQ_OK) return st;
   if (E < 1) return fail(BSQ_ERR_INVALID_ARG, "%s: E must be >= 1", what);
   if (E > bsq::kMaxExperts) return fail(BSQ_ERR_UNSUPPORTED, "%s: E > %d", what, bsq::kMaxExperts);
@@ -307,7 +353,7 @@ bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N, int32_t
                              const void* x_scale, const float* x_tensor_scale, int64_t K, const int32_t* offsets,
                              int64_t E, void* grad_w, void* stream) {
   const char* what = "bsq_grouped_wgrad";
-  bsq_status st = check_gemm_common(what, grad_out, S, N, x_fmt, K, grad_w);
+  bsq_status st = check_gemm_common(what, grad_out, S, N, x_fmt, K, grad_w, E * N * K);
   if (st != BSQ_OK) return st;
   if (E < 1) return fail(BSQ_ERR_INVALID_ARG, "%s: E must be >= 1", what);
   if (E > bsq::kMaxExperts) return fail(BSQ_ERR_UNSUPPORTED, "%s: E > %d", what, bsq::kMaxExperts);

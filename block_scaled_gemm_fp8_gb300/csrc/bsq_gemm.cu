@@ -57,6 +57,7 @@
 // peer CTA) instead of hanging.
 #include <atomic>
 #include <cstdlib>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -159,7 +160,7 @@ struct SharedTail {
   uint32_t sink;                  // target of the odd CTA's st.async announcements (never read)
   uint32_t abort_flag;
   int32_t total_tiles;
-  int32_t pad;
+  int32_t first_tiles;             // tiles of the first GEMM of the launch
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
@@ -260,9 +261,8 @@ __device__ __forceinline__ TileInfo decode_tile(int t, ExpertCursor& c, const Pa
 // Width of the pair MMA for a tile with n_valid columns.  CTA r stages grad_out n rows
 // [r*Nm/2, (r+1)*Nm/2); the 3-D grad_out box (wgrad, b_mode 2) needs Nm/2 to be a whole
 // number of 64-column swizzle atoms.
-template <int OP>
-__device__ __forceinline__ int mma_width(int n_valid, int b_mode) {
-  if (OP == kWgrad && b_mode == 2) return n_valid > 128 ? 256 : 128;
+__device__ __forceinline__ int mma_width(bool dgrad, int n_valid, int b_mode) {
+  if (!dgrad && b_mode == 2) return n_valid > 128 ? 256 : 128;
   return max(32, (n_valid + 15) & ~15);
 }
 
@@ -328,13 +328,47 @@ __device__ __forceinline__ void drain_pending(uint64_t* full, uint32_t mask, uin
     }
 }
 
-template <int FMT, int OP, bool SHORT>
+// One GEMM of a launch: its tensor maps (packed operand, grad_out, FP4 scale tiles) and
+// parameters (host side; the kernel takes them as separate arguments).
+struct OpArgs {
+  CUtensorMap tm_p;
+  CUtensorMap tm_g;
+  CUtensorMap tm_s;
+  Params p;
+};
+
+// Tile t of a launch: whether it belongs to the second GEMM (kBoth) and its coordinates;
+// each role keeps its own expert cursors (c0 over the first GEMM's tiles, c1 the second's).
+template <int OPS>
+__device__ __forceinline__ TileInfo tile_at(int t, int n_first, ExpertCursor& c0, ExpertCursor& c1, const Params& p0,
+                                            const Params& p1, int rank, bool& second) {
+  second = OPS == kBoth && t >= n_first;
+  if (second) return decode_tile<kWgrad>(t - n_first, c1, p1, rank);
+  return decode_tile<OPS == kBoth ? static_cast<int>(kDgrad) : OPS>(t, c0, p0, rank);
+}
+
+template <typename T>
+__device__ __forceinline__ T pick(bool second, T first_value, T second_value) {
+  return second ? second_value : first_value;
+}
+
+// One launch runs the tiles of one GEMM (OPS = kDgrad or kWgrad, described by a0) or of two
+// (OPS = kBoth: the dgrad tiles of a0, then the wgrad tiles of a1, over the same grad_out,
+// packed operands of one format and the same expert offsets).  Every role walks the same
+// tile sequence; `second` marks a tile of a1.
+template <int FMT, int OPS, bool SHORT>
 __global__ void __launch_bounds__(kThreads, 1)
-    bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_g,
-                    const __grid_constant__ CUtensorMap tm_s, const Params p) {
+    bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p0, const __grid_constant__ CUtensorMap tm_g0,
+                    const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_p1,
+                    const __grid_constant__ CUtensorMap tm_g1, const __grid_constant__ CUtensorMap tm_s1,
+                    const Params p, const Params p1) {
   using F = Fmt<FMT>;
   using R = Roles<SHORT>;
+  constexpr int OP0 = OPS == kBoth ? static_cast<int>(kDgrad) : OPS;
   static_assert(!SHORT || FMT != BSQ_BF16, "the short-tile kernel decodes packed formats only");
+  static_assert(!SHORT || OPS == kWgrad, "the short-tile kernel runs wgrad launches only");
+  // p: the first GEMM, and the fields both GEMMs share (offsets, E, S, N, Kc, tiling, error
+  // word, wait limit); p1: the second GEMM of a kBoth launch.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring_b = smem;
@@ -368,9 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&tm_p);
-    tma_prefetch_map(&tm_g);
-    if (F::kFp4 && p.scale_tma) tma_prefetch_map(&tm_s);
+    tma_prefetch_map(&tm_p0);
+    tma_prefetch_map(&tm_g0);
+    if (F::kFp4 && p.scale_tma) tma_prefetch_map(&tm_s0);
+    if (OPS == kBoth) {
+      tma_prefetch_map(&tm_p1);
+      tma_prefetch_map(&tm_g1);
+      if (F::kFp4 && p1.scale_tma) tma_prefetch_map(&tm_s1);
+    }
   }
   if (warp == 2) {
     tmem_alloc_pair(smem_u32(&sh.tmem_base), kTmemCols);
@@ -381,18 +420,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Validate the offsets and count the tiles: lane l owns experts [l*per, (l+1)*per).
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int bad = 0, sum = 0;
+    int bad = 0, sum0 = 0, sum1 = 0;
     int a = e0 == 0 ? 0 : expert_end(p, e0 - 1);
     for (int e = e0; e < e1; ++e) {
       const int b = expert_end(p, e);
       if (b < a || b > p.S || a < 0) bad = 1;
-      sum += expert_tiles<OP>(p, max(b - a, 0));
+      sum0 += expert_tiles<OP0>(p, max(b - a, 0));
+      if (OPS == kBoth) sum1 += expert_tiles<kWgrad>(p1, max(b - a, 0));
       a = b;
     }
     bad = __any_sync(0xffffffffu, bad);
-    const int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(sum)));
+    const int t0 = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(sum0)));
+    const int t1 = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(sum1)));
     if (lane == 0) {
-      sh.total_tiles = bad ? 0 : total;
+      sh.total_tiles = bad ? 0 : t0 + t1;
+      sh.first_tiles = t0;
       if (bad && blockIdx.x == 0) record_error(p.err, BSQ_DEVERR_BAD_OFFSETS);
     }
   }
@@ -402,23 +444,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();   // both CTAs of the pair have initialised their barriers before any remote arrival
   const uint32_t tmem_base = sh.tmem_base;
   const int total_tiles = sh.total_tiles;
+  const int n_first = sh.first_tiles;
   const uint64_t limit = p.timeout_ns;
   const int rank = static_cast<int>(cluster_ctarank());
   const int cl_id = blockIdx.x / kPair, n_cl = gridDim.x / kPair;
   uint32_t mma_acc_uses = 0;   // MMA thread: tiles accumulated (accumulator buffer b: uses of b)
+  // Tile t of the launch: whether it belongs to a1 (second) and its coordinates; each role
+  // keeps its own expert cursors (c0 over a0's tiles, c1 over a1's).
+  auto is_dgrad = [](bool second) { return !second && OP0 == kDgrad; };
 
   // ---------------------------------------------------------------- roles
   if (warp == 0) {
     // ===== TMA producer: packed ring, one unit (two k-blocks) per barrier =====
     if (lane == 0) {
       uint32_t uc = 0;
-      ExpertCursor cur = cursor_begin<OP>(p);
+      ExpertCursor c0 = cursor_begin<OP0>(p), c1 = cursor_begin<kWgrad>(p1);
       uint32_t pend_mask = 0, pend_par = 0;
-      const uint32_t kb_bytes = F::kPBytes + ((F::kFp4 && p.scale_tma) ? F::kSBytes : 0);
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
+        bool second;
+        const TileInfo ti = tile_at<OPS>(t, n_first, c0, c1, p, p1, rank, second);
+        const bool dg = is_dgrad(second);
+        const CUtensorMap* tm_p = second ? &tm_p1 : &tm_p0;
+        const CUtensorMap* tm_s = second ? &tm_s1 : &tm_s0;
+        const bool scale_tma = F::kFp4 && pick(second, p.scale_tma, p1.scale_tma) != 0;
+        const uint32_t kb_bytes = F::kPBytes + (scale_tma ? F::kSBytes : 0);
         const int m0 = ti.mt * kTileM;
-        const int pbatch = OP == kDgrad ? ti.e : 0;
+        const int pbatch = dg ? ti.e : 0;
         const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
         bool ok = true;
         for (int j = 0; j < units; ++j, ++uc) {
@@ -431,17 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
           for (int h = 0; h < nk; ++h) {
             const int kb = kUnitKb * j + h;
-            const int prow = OP == kDgrad ? kb * kTileK : ti.r0 + kb * kTileK;
+            const int prow = dg ? kb * kTileK : ti.r0 + kb * kTileK;
             uint8_t* dst = ring_p + sl.idx * F::kPUnitBytes + h * F::kPStageBytes;
             if (FMT == BSQ_BF16) {
-              tma_load_3d(smem_u32(dst), &tm_p, full, m0, prow, pbatch);
-              tma_load_3d(smem_u32(dst + kBoxBytes), &tm_p, full, m0 + 64, prow, pbatch);
+              tma_load_3d(smem_u32(dst), tm_p, full, m0, prow, pbatch);
+              tma_load_3d(smem_u32(dst + kBoxBytes), tm_p, full, m0 + 64, prow, pbatch);
             } else {
-              tma_load_3d(smem_u32(dst), &tm_p, full, FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2, prow, pbatch);
-              if (F::kFp4 && p.scale_tma) {
+              tma_load_3d(smem_u32(dst), tm_p, full, FMT == BSQ_FP8_E4M3_B128 ? m0 : m0 / 2, prow, pbatch);
+              if (scale_tma) {
                 // 16-byte aligned window holding this tile's scales (4 or 8 bytes per row)
                 const int xs = (FMT == BSQ_MXFP4 ? (m0 >> 5) : (m0 >> 4)) & ~15;
-                tma_load_3d(smem_u32(dst + F::kPBytes), &tm_s, full, xs, prow, pbatch);
+                tma_load_3d(smem_u32(dst + F::kPBytes), tm_s, full, xs, prow, pbatch);
               }
             }
           }
@@ -454,13 +505,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ===== TMA producer: this CTA's half of the grad_out ring, one unit at a time =====
     if (lane == 0) {
       uint32_t uc = 0;
-      ExpertCursor cur = cursor_begin<OP>(p);
+      ExpertCursor c0 = cursor_begin<OP0>(p), c1 = cursor_begin<kWgrad>(p1);
       uint32_t pend_mask = 0, pend_par = 0;
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
-        const int half = rank * (mma_width<OP>(ti.n_valid, p.b_mode) / 2);   // first n of this CTA's half
+        bool second;
+        const TileInfo ti = tile_at<OPS>(t, n_first, c0, c1, p, p1, rank, second);
+        const bool dg = is_dgrad(second);
+        const CUtensorMap* tm_g = second ? &tm_g1 : &tm_g0;
+        const int b_mode = pick(second, p.b_mode, p1.b_mode);
+        const int b_rows = pick(second, p.b_rows, p1.b_rows);
+        const int half = rank * (mma_width(dg, ti.n_valid, b_mode) / 2);   // first n of this CTA's half
         // bytes of one k-block's half tile
-        const uint32_t kb_bytes = p.b_mode == 1 ? p.b_rows * 128 : (p.b_mode == 2 ? p.b_rows : 2) * kBoxBytes;
+        const uint32_t kb_bytes = b_mode == 1 ? b_rows * 128 : (b_mode == 2 ? b_rows : 2) * kBoxBytes;
         const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
         bool ok = true;
         for (int j = 0; j < units; ++j, ++uc) {
@@ -474,16 +530,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < nk; ++h) {
             const int kb = kUnitKb * j + h;
             const uint32_t dst = smem_u32(ring_b + sl.idx * kBUnitBytes + h * kBBytes);
-            if (p.b_mode == 1) {
+            if (b_mode == 1) {
               // dgrad: b_rows tokens x 64 columns, K-major rows of 128 bytes
-              tma_load_2d(dst, &tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + half);
-            } else if (p.b_mode == 2) {
+              tma_load_2d(dst, tm_g, full, kb * kTileK, ti.r0 + ti.nt * kTileN + half);
+            } else if (b_mode == 2) {
               // wgrad: b_rows swizzle atoms x 64 tokens x 64 columns
-              tma_load_3d(dst, &tm_g, full, 0, ti.r0 + kb * kTileK, (ti.nt * kTileN + half) / 64);
+              tma_load_3d(dst, tm_g, full, 0, ti.r0 + kb * kTileK, (ti.nt * kTileN + half) / 64);
             } else {
               // wgrad, N not a multiple of 64: two 64 x 64 boxes (the second may lie past N)
               for (int b = 0; b < 2; ++b)
-                tma_load_2d(dst + b * kBoxBytes, &tm_g, full, ti.nt * kTileN + half + 64 * b, ti.r0 + kb * kTileK);
+                tma_load_2d(dst + b * kBoxBytes, tm_g, full, ti.nt * kTileN + half + 64 * b, ti.r0 + kb * kTileK);
             }
           }
         }
@@ -499,34 +555,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // by adding to the 14-bit start-address field (addresses < 256 KB).
     if (lane == 0 && rank == 0) {
       uint32_t iu = 0, pu = 0;   // ring slot and phase parity of the next unit
-      ExpertCursor cur = cursor_begin<OP>(p);
+      ExpertCursor c0 = cursor_begin<OP0>(p), c1 = cursor_begin<kWgrad>(p1);
       uint32_t& acc = mma_acc_uses;
-      const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), kBoxBytes, 1024);   // A: MN-major, atoms of 64 m at 8 KB
-      const uint64_t bdesc0 = OP == kDgrad ? sdesc_sw128(smem_u32(ring_b), 16, 1024)          // B: K-major rows
-                                           : sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B: MN-major
-      constexpr uint32_t kBStep = OP == kDgrad ? (32 >> 4) : (2048 >> 4);   // 16 k of the B tile
+      const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), kBoxBytes, 1024);    // A: MN-major, atoms of 64 m at 8 KB
+      const uint64_t bdesc_k = sdesc_sw128(smem_u32(ring_b), 16, 1024);          // B (dgrad): K-major rows
+      const uint64_t bdesc_mn = sdesc_sw128(smem_u32(ring_b), kBoxBytes, 1024);  // B (wgrad): MN-major
       const uint32_t a_full0 = smem_u32(&sh.a_full[0]), op_empty0 = smem_u32(&sh.op_empty[0]);
-      // A unit is ready once both CTAs' relays have arrived: each has seen its CTA's A rows
-      // written and its grad_out half landed, and released them at cluster scope.
+      // A unit is ready once both CTAs' relays have announced it: each has seen its CTA's A
+      // rows written and its grad_out half landed.
       auto ready = [&](uint32_t s, uint32_t q) { return wait_phase<true>(a_full0 + 8 * s, q, abort_flag, p.err, limit); };
-      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
-        if (ti.kblocks == 0) continue;
-        const uint32_t buf = acc & 1u;
-        const uint32_t acc_phase = (acc >> 1) & 1u;
-        if (!wait_phase<true>(smem_u32(&sh.tmem_empty[buf]), acc_phase ^ 1u, abort_flag, p.err, limit)) break;
-        tc_fence_after();
-        const uint32_t n_mma = static_cast<uint32_t>(mma_width<OP>(ti.n_valid, p.b_mode));
-        const uint32_t idesc = idesc_bf16_f32(kPair * kTileM, n_mma, true, OP == kWgrad);
-        const uint32_t d_tmem = tmem_base + buf * kTileN;
-        const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
-        // Each unit's MMAs are queued, then the next unit is awaited while they run, then
-        // the commit that frees the unit's slots (a commit takes a slot of the tensor
-        // instruction queue; waiting after it would leave the pipe idle).  The next unit's
-        // slots were freed by a commit issued at least one unit earlier.
+      // The units of one tile; BSTEP is the B descriptor step per 16 k (K-major: 32 bytes,
+      // MN-major: one 2 KB row group).  Each unit's MMAs are queued, then the next unit is
+      // awaited while they run, then the commit that frees the unit's slots (a commit takes
+      // a slot of the tensor instruction queue; waiting after it would leave the pipe idle).
+      // The next unit's slots were freed by a commit issued at least one unit earlier.
+      auto run_tile = [&](auto bstep, uint64_t bdesc0, uint32_t d_tmem, uint32_t idesc, int kblocks) {
+        constexpr uint32_t kBStep = decltype(bstep)::value;
+        const int units = (kblocks + kUnitKb - 1) / kUnitKb;
         bool ok = ready(iu, pu);
         for (int j = 0; ok && j < units; ++j) {
-          const int nk = min(kUnitKb, ti.kblocks - kUnitKb * j);
+          const int nk = min(kUnitKb, kblocks - kUnitKb * j);
           tc_fence_after();
           const uint64_t ad = adesc0 + iu * (kAUnitBytes >> 4);
           const uint64_t bd = bdesc0 + iu * (kBUnitBytes >> 4);
@@ -545,6 +593,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < units) ok = ready(iu, pu);
           umma_commit_pair(op_empty0 + 8 * su, kPairMask);
         }
+        return ok;
+      };
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        bool second;
+        const TileInfo ti = tile_at<OPS>(t, n_first, c0, c1, p, p1, rank, second);
+        if (ti.kblocks == 0) continue;
+        const bool dg = is_dgrad(second);
+        const uint32_t buf = acc & 1u;
+        const uint32_t acc_phase = (acc >> 1) & 1u;
+        if (!wait_phase<true>(smem_u32(&sh.tmem_empty[buf]), acc_phase ^ 1u, abort_flag, p.err, limit)) break;
+        tc_fence_after();
+        const uint32_t n_mma = static_cast<uint32_t>(mma_width(dg, ti.n_valid, pick(second, p.b_mode, p1.b_mode)));
+        const uint32_t idesc = idesc_bf16_f32(kPair * kTileM, n_mma, true, !dg);
+        const uint32_t d_tmem = tmem_base + buf * kTileN;
+        const bool ok = dg ? run_tile(std::integral_constant<uint32_t, (32 >> 4)>{}, bdesc_k, d_tmem, idesc, ti.kblocks)
+                           : run_tile(std::integral_constant<uint32_t, (2048 >> 4)>{}, bdesc_mn, d_tmem, idesc, ti.kblocks);
         if (!ok) break;
         umma_commit_pair(smem_u32(&sh.tmem_full[buf]), kPairMask);
         ++acc;
@@ -558,10 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // CTA's MMA thread issues the MMA that reads the odd CTA's operands.
     if (lane == 0) {
       uint32_t uc = 0;
-      ExpertCursor cur = cursor_begin<OP>(p);
+      ExpertCursor c0 = cursor_begin<OP0>(p), c1 = cursor_begin<kWgrad>(p1);
       const uint32_t a_full0 = smem_u32(&sh.a_full[0]);
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-        const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
+        bool second;
+        const TileInfo ti = tile_at<OPS>(t, n_first, c0, c1, p, p1, rank, second);
         const int units = (ti.kblocks + kUnitKb - 1) / kUnitKb;
         bool ok = true;
         for (int j = 0; j < units; ++j, ++uc) {
@@ -585,17 +650,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = R::kEpiPerQuarter > 1 ? (warp - 4) >> 2 : 0;   // 0 .. kEpiPerQuarter-1
     const int i = q * 32 + lane;              // accumulator row = tile m index (permuted)
     const int mcol = lane_to_col<FMT>(i);
-    ExpertCursor cur = cursor_begin<OP>(p);
+    ExpertCursor c0 = cursor_begin<OP0>(p), c1 = cursor_begin<kWgrad>(p1);
     uint32_t acc = 0;
     for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-      const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
+      bool second;
+      const TileInfo ti = tile_at<OPS>(t, n_first, c0, c1, p, p1, rank, second);
       const int m = ti.mt * kTileM + mcol;
       const bool mok = m < p.Kc;
-      __nv_bfloat16* obase;
-      if (OP == kDgrad)
-        obase = p.out + static_cast<int64_t>(ti.r0 + ti.nt * kTileN) * p.Kc + m;
+      __nv_bfloat16* obase = pick(second, p.out, p1.out);
+      if (is_dgrad(second))
+        obase += static_cast<int64_t>(ti.r0 + ti.nt * kTileN) * p.Kc + m;
       else
-        obase = p.out + ti.e * p.out_expert_stride + static_cast<int64_t>(ti.nt * kTileN) * p.Kc + m;
+        obase += ti.e * pick(second, p.out_expert_stride, p1.out_expert_stride) +
+                 static_cast<int64_t>(ti.nt * kTileN) * p.Kc + m;
       if (ti.kblocks == 0) {
         // wgrad of an expert without rows: exact zeros
         const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
@@ -662,15 +729,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t p_off = F::kFp4 ? r * F::kPRowBytes + 16 * g : r * F::kPRowBytes + 32 * g + 16 * (r & 1);
     uint32_t uc = 0;   // units of earlier tiles: ring position of this tile's unit 0
-    ExpertCursor cur = cursor_begin<OP>(p);
-    for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
-      const TileInfo ti = decode_tile<OP>(t, cur, p, rank);
+    // One tile of the GEMM described by gp (a dgrad or a wgrad, fixed at compile time so
+    // that the per-k-block work has no run-time op selection); false when the CTA aborted.
+    auto deq_tile = [&](auto op_c, const TileInfo& ti, const Params& gp) -> bool {
+      constexpr int OP = decltype(op_c)::value;
       const int m0 = ti.mt * kTileM;
       const int col0 = m0 + 32 * g;
       const bool col_ok = col0 < p.Kc;
       const int pbatch = OP == kDgrad ? ti.e : 0;
       float tscale = 0.f;
-      if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + pbatch);
+      if (FMT == BSQ_NVFP4) tscale = __ldg(gp.tensor_scale + pbatch);
       // this thread's scale byte(s) inside the staged 16-byte scale window of row r
       const uint32_t s_off = F::kPBytes + r * 16 + (FMT == BSQ_MXFP4 ? ((m0 >> 5) & 15) + g : ((m0 >> 4) & 15) + 2 * g);
       bool ok = true;
@@ -695,16 +763,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           sraw[ps] = 0;
           sf[ps] = 0.f;
           if (valid[ps]) {
-            const int64_t grow = static_cast<int64_t>(pbatch) * p.p_rows + prow0 + rr;
+            const int64_t grow = static_cast<int64_t>(pbatch) * gp.p_rows + prow0 + rr;
             if (FMT == BSQ_FP8_E4M3_B128)
-              sf[ps] = __ldg(reinterpret_cast<const float*>(p.scale) +
-                             (static_cast<int64_t>(pbatch) * p.scale_rblocks + ((prow0 + rr) >> 7)) * p.scale_ld +
+              sf[ps] = __ldg(reinterpret_cast<const float*>(gp.scale) +
+                             (static_cast<int64_t>(pbatch) * gp.scale_rblocks + ((prow0 + rr) >> 7)) * p.scale_ld +
                              (col0 >> 7));
-            else if (FMT == BSQ_MXFP4 && !p.scale_tma)
-              sraw[ps] = __ldg(p.scale + grow * p.scale_ld + (col0 >> 5));
-            else if (FMT == BSQ_NVFP4 && !p.scale_tma)
-              sraw[ps] = static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4))) |
-                         (static_cast<uint32_t>(__ldg(p.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
+            else if (FMT == BSQ_MXFP4 && !gp.scale_tma)
+              sraw[ps] = __ldg(gp.scale + grow * p.scale_ld + (col0 >> 5));
+            else if (FMT == BSQ_NVFP4 && !gp.scale_tma)
+              sraw[ps] = static_cast<uint32_t>(__ldg(gp.scale + grow * p.scale_ld + (col0 >> 4))) |
+                         (static_cast<uint32_t>(__ldg(gp.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
           }
         }
         // Both teams wait on every phase of the packed slot (in unit order) and both count
@@ -723,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t po = p_off + ps * R::kRowStep * F::kPRowBytes;
           if (FMT != BSQ_BF16 && valid[ps]) {
             if (F::kFp4) {
-              if (p.scale_tma) {
+              if (gp.scale_tma) {
                 const uint32_t so = s_off + ps * R::kRowStep * 16;
                 sraw[ps] = FMT == BSQ_MXFP4 ? lds_u8(pst + so) : lds_u16(pst + so);
               }
@@ -787,8 +855,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.a_local[sa.idx]));   // this CTA's relay passes it on
       }
-      if (!ok) break;
       uc += units;
+      return ok;
+    };
+    // The first GEMM's tiles, then (kBoth) the second's: two loops, so that only one expert
+    // cursor is live at a time.
+    int t = cl_id;
+    bool ok = true;
+    {
+      ExpertCursor c0 = cursor_begin<OP0>(p);
+      const int end0 = OPS == kBoth ? n_first : total_tiles;
+      for (; ok && t < end0 && !*abort_flag; t += n_cl)
+        ok = deq_tile(std::integral_constant<int, OP0>{}, decode_tile<OP0>(t, c0, p, rank), p);
+    }
+    if (OPS == kBoth) {
+      ExpertCursor c1 = cursor_begin<kWgrad>(p1);
+      for (; ok && t < total_tiles && !*abort_flag; t += n_cl)
+        ok = deq_tile(std::integral_constant<int, kWgrad>{}, decode_tile<kWgrad>(t - n_first, c1, p1, rank), p1);
     }
   }
 
@@ -859,20 +942,21 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const voi
 
 namespace {
 
-template <int FMT, int OP>
-int launch_typed(const GemmArgs& a, const char** msg) {
-  using F = Fmt<FMT>;
-  CUtensorMap tm_p, tm_g;
+// Tensor maps and parameters of one GEMM; *bound is an upper bound of its pair tiles (the
+// exact count depends on the offsets, which only the device reads).
+template <int FMT>
+int prepare_op(const GemmArgs& a, OpArgs& o, int64_t* bound, const char** msg) {
+  const bool dgrad = a.op == kDgrad;
   int b_mode = 0, b_rows = 0;
   {
     // this CTA's half of a k-block's grad_out tile in a single TMA copy where the shape allows it
     const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.S)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
     bool ok = false;
-    if (OP == kDgrad) {
+    if (dgrad) {
       b_rows = static_cast<int>(a.S < kBHalf ? a.S : kBHalf);
       const uint32_t box[2] = {64, static_cast<uint32_t>(b_rows)};
-      ok = encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_map(&o.tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
       b_mode = 1;
     } else if (a.N % 64 == 0) {
       // [N/64 swizzle columns][S tokens][64 columns] view of grad_out
@@ -880,12 +964,12 @@ int launch_typed(const GemmArgs& a, const char** msg) {
       const uint64_t d3[3] = {64, static_cast<uint64_t>(a.S), static_cast<uint64_t>(a.N / 64)};
       const uint64_t s3[2] = {static_cast<uint64_t>(a.N) * 2, 128};
       const uint32_t box[3] = {64, 64, static_cast<uint32_t>(b_rows)};
-      ok = encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.g, d3, s3, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_map(&o.tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.g, d3, s3, box, CU_TENSOR_MAP_SWIZZLE_128B);
       b_mode = 2;
     }
-    if (!ok && OP != kDgrad) {
+    if (!ok && !dgrad) {
       const uint32_t box[2] = {64, 64};
-      ok = encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_map(&o.tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
       b_mode = 0;
     }
     if (!ok) {
@@ -909,13 +993,13 @@ int launch_typed(const GemmArgs& a, const char** msg) {
     const uint64_t dims[3] = {inner, static_cast<uint64_t>(a.p_rows), static_cast<uint64_t>(a.p_batch)};
     const uint64_t strides[2] = {row_bytes, row_bytes * static_cast<uint64_t>(a.p_rows)};
     const uint32_t box[3] = {box0, static_cast<uint32_t>(kTileK), 1};
-    if (!encode_map(&tm_p, dt, 3, a.p_data, dims, strides, box, sw)) {
+    if (!encode_map(&o.tm_p, dt, 3, a.p_data, dims, strides, box, sw)) {
       *msg = "tensor map encoding failed for the packed operand";
       return -1;
     }
   }
   // FP4 scale tiles through TMA when the scale row pitch is a multiple of 16 bytes.
-  CUtensorMap tm_s = tm_p;
+  o.tm_s = o.tm_p;
   int scale_tma = 0;
   if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) {
     const uint64_t srow = FMT == BSQ_MXFP4 ? a.kc / 32 : a.kc / 16;
@@ -923,7 +1007,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
       const uint64_t dims[3] = {srow, static_cast<uint64_t>(a.p_rows), static_cast<uint64_t>(a.p_batch)};
       const uint64_t strides[2] = {srow, srow * static_cast<uint64_t>(a.p_rows)};
       const uint32_t box[3] = {16, static_cast<uint32_t>(kTileK), 1};
-      if (!encode_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.p_scale, dims, strides, box,
+      if (!encode_map(&o.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.p_scale, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE)) {
         *msg = "tensor map encoding failed for the scales";
         return -1;
@@ -931,7 +1015,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
       scale_tma = 1;
     }
   }
-  Params p;
+  Params& p = o.p;
   p.scale_tma = scale_tma;
   p.b_mode = b_mode;
   p.b_rows = b_rows;
@@ -940,7 +1024,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   p.offsets = a.offsets;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.err = a.err;
-  p.out_expert_stride = OP == kWgrad ? a.N * a.kc : 0;
+  p.out_expert_stride = dgrad ? 0 : a.N * a.kc;
   p.p_rows = a.p_rows;
   p.E = static_cast<int32_t>(a.E);
   p.S = static_cast<int32_t>(a.S);
@@ -953,22 +1037,38 @@ int launch_typed(const GemmArgs& a, const char** msg) {
                                   : static_cast<int32_t>((a.kc + 127) / 128);
   p.scale_rblocks = static_cast<int32_t>((a.p_rows + 127) / 128);
   p.timeout_ns = wait_limit_ns();
-
-  // Upper bound of the pair-tile count (the exact count depends on the offsets, read on the device).
   const int64_t nn = (a.N + kTileN - 1) / kTileN;
-  const int64_t bound = OP == kDgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
+  *bound = dgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
+  return 0;
+}
+
+// Launch one GEMM (OPS = its op; ops[0]) or a dgrad and a wgrad over the same grad_out
+// (OPS = kBoth; ops[0] the dgrad, ops[1] the wgrad).
+template <int FMT, int OPS>
+int launch_typed(const GemmArgs* ops, const char** msg) {
+  using F = Fmt<FMT>;
+  OpArgs a0, a1;
+  int64_t b0 = 0, b1 = 0;
+  if (prepare_op<FMT>(ops[0], a0, &b0, msg) != 0) return -1;
+  if (OPS == kBoth) {
+    if (prepare_op<FMT>(ops[1], a1, &b1, msg) != 0) return -1;
+  } else {
+    a1 = a0;
+  }
+  const int64_t bound = b0 + b1;
+  const GemmArgs& a = ops[0];
   static_assert(F::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
   // Kernel: wgrad of a packed format whose groups average fewer than 1024 rows (a tile of
   // at most 16 k-blocks, where the epilogue sets the pace) takes the short-tile variant
   // (more epilogue warps).  BSQ_GEMM_SHORT_TILES=1 / 0 forces one or the other.
-  auto kern = bsq_gemm_kernel<FMT, OP, false>;
+  auto kern = bsq_gemm_kernel<FMT, OPS, false>;
   bool short_tiles = false;
-  if constexpr (OP == kWgrad && FMT != BSQ_BF16) {
+  if constexpr (OPS == kWgrad && FMT != BSQ_BF16) {
     const char* env = std::getenv("BSQ_GEMM_SHORT_TILES");
     if (env && (env[0] == '0' || env[0] == '1')) short_tiles = env[0] == '1';
     else short_tiles = a.S < 1024 * a.E;
-    if (short_tiles) kern = bsq_gemm_kernel<FMT, OP, true>;
+    if (short_tiles) kern = bsq_gemm_kernel<FMT, OPS, true>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -1001,7 +1101,8 @@ int launch_typed(const GemmArgs& a, const char** msg) {
   int64_t clusters = bound < max_clusters ? bound : max_clusters;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kPair));
-  if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, tm_p, tm_g, tm_s, p);
+  if (e == cudaSuccess)
+    e = cudaLaunchKernelEx(&cfg, kern, a0.tm_p, a0.tm_g, a0.tm_s, a1.tm_p, a1.tm_g, a1.tm_s, a0.p, a1.p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);
@@ -1014,7 +1115,7 @@ int launch_typed(const GemmArgs& a, const char** msg) {
 
 int launch_gemm(const GemmArgs& a, const char** msg) {
 #define BSQ_CASE(F_, O_) \
-  if (a.fmt == F_ && a.op == O_) return launch_typed<F_, O_>(a, msg);
+  if (a.fmt == F_ && a.op == O_) return launch_typed<F_, O_>(&a, msg);
   BSQ_CASE(BSQ_BF16, kDgrad)
   BSQ_CASE(BSQ_BF16, kWgrad)
   BSQ_CASE(BSQ_FP8_E4M3_B128, kDgrad)
@@ -1025,6 +1126,25 @@ int launch_gemm(const GemmArgs& a, const char** msg) {
   BSQ_CASE(BSQ_NVFP4, kWgrad)
 #undef BSQ_CASE
   *msg = "unsupported format/op";
+  return -1;
+}
+
+int launch_gemm_backward(const GemmArgs& dgrad, const GemmArgs& wgrad, const char** msg) {
+  if (dgrad.op != kDgrad || wgrad.op != kWgrad || dgrad.fmt != wgrad.fmt || dgrad.E != wgrad.E ||
+      dgrad.S != wgrad.S || dgrad.N != wgrad.N || dgrad.kc != wgrad.kc || dgrad.g != wgrad.g ||
+      dgrad.offsets != wgrad.offsets) {
+    *msg = "a fused backward needs one grad_out, one packed format, one K and one set of offsets";
+    return -1;
+  }
+  const GemmArgs ops[2] = {dgrad, wgrad};
+  switch (dgrad.fmt) {
+    case BSQ_BF16: return launch_typed<BSQ_BF16, kBoth>(ops, msg);
+    case BSQ_FP8_E4M3_B128: return launch_typed<BSQ_FP8_E4M3_B128, kBoth>(ops, msg);
+    case BSQ_MXFP4: return launch_typed<BSQ_MXFP4, kBoth>(ops, msg);
+    case BSQ_NVFP4: return launch_typed<BSQ_NVFP4, kBoth>(ops, msg);
+    default: break;
+  }
+  *msg = "unsupported format";
   return -1;
 }
 

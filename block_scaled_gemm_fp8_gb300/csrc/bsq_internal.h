@@ -8,7 +8,7 @@
 
 namespace bsq {
 
-enum GemmOp : int { kDgrad = 0, kWgrad = 1 };
+enum GemmOp : int { kDgrad = 0, kWgrad = 1, kBoth = 2 };   // kBoth: one launch, dgrad tiles then wgrad tiles
 
 // Fixed tile shape of the fused kernel (see bsq_gemm.cu):
 //   M side (tensor-memory lanes): 128 columns of the packed operand's contiguous axis
@@ -42,6 +42,9 @@ struct GemmArgs {
 
 // Returns a cudaError_t-style code (0 = launched) and fills `msg` on failure.
 int launch_gemm(const GemmArgs& a, const char** msg);
+// One launch for a dgrad and a wgrad over the same grad_out (one packed format, one K):
+// the dgrad's tiles, then the wgrad's.
+int launch_gemm_backward(const GemmArgs& dgrad, const GemmArgs& wgrad, const char** msg);
 
 struct DequantArgs {
   int fmt;

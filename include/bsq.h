@@ -116,6 +116,33 @@ bsq_status bsq_linear_wgrad(const void* grad_out, int64_t M, int64_t N,
                             int32_t x_fmt, const void* x_data, const void* x_scale,
                             const float* x_tensor_scale, int64_t K, void* grad_w, void* stream);
 
+/* Bits of `needs` in bsq_linear_backward: which gradients the caller wants. */
+#define BSQ_NEEDS_GRAD_X 1u   /* grad_x = grad_out @ deq(W) */
+#define BSQ_NEEDS_GRAD_W 2u   /* grad_w = grad_out^T @ deq(X) */
+
+/*
+ * bsq_linear_backward -- both gradients of a linear layer from one grad_out, with output
+ * masks: AstrAI `astrai/extension/fp8.py`, `_LinearFp8.backward` (the gradient is shared by
+ * dX and dW; `ctx.needs_input_grad` decides which of the two products run), applied to the
+ * dequantize-then-BF16-matmul backward of MSLK PR #393, Implementation Method:
+ *     grad_x[M][K] = grad_out[M][N] @ deq(W)[N][K]        (if needs & BSQ_NEEDS_GRAD_X)
+ *     grad_w[N][K] = grad_out[M][N]^T @ deq(X)[M][K]      (if needs & BSQ_NEEDS_GRAD_W)
+ * W: packed [1][N][K] in w_fmt; X: packed [1][M][K] in x_fmt (BSQ_BF16 allowed for either).
+ * Arguments of a product that is not wanted are not read and may be null.  With both
+ * products, the same packed format for W and X and M > 16, one persistent launch computes
+ * the dgrad tiles and then the wgrad tiles, so grad_out streams through the L2 once for
+ * both; otherwise the call behaves as bsq_linear_dgrad followed by bsq_linear_wgrad on the
+ * stream.  Every output element equals the corresponding single-product entry point's
+ * (the same tiles in the same accumulation order).  needs == 0 returns BSQ_OK and does
+ * nothing; unknown bits return BSQ_ERR_INVALID_ARG.
+ */
+bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N,
+                               int32_t w_fmt, const void* w_data, const void* w_scale,
+                               const float* w_tensor_scale,
+                               int32_t x_fmt, const void* x_data, const void* x_scale,
+                               const float* x_tensor_scale,
+                               int64_t K, uint32_t needs, void* grad_x, void* grad_w, void* stream);
+
 /*
  * bsq_grouped_dgrad -- per expert e, grad_x[r0:r1] = grad_out[r0:r1] @ deq(W[e])
  * (transformers PR #50031 FP8GroupedMatmulFunction.backward).

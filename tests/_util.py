@@ -75,11 +75,16 @@ def deq_cols(p, cols, b=0):
     return D.dequant_cols(ORACLE_FMT[p.fmt], d, s, ts, p.rows, p.cols, cols, b, p.batch)
 
 
-def run_config(c, outs=None):
-    """Launch every op of a workload (bsq_*), into `outs` when given; returns the outputs."""
+def run_config(c, outs=None, fused=True):
+    """Launch every op of a workload (bsq_*), into `outs` when given; returns the outputs.
+    A linear workload runs as one bsq_linear_backward call (as bench.py times it) unless
+    fused is False, which calls bsq_linear_dgrad and bsq_linear_wgrad."""
     from block_scaled_gemm_fp8_gb300 import bsq
     outs = {} if outs is None else outs
-    if not c["grouped"]:
+    if not c["grouped"] and fused:
+        outs["dgrad"], outs["wgrad"] = bsq.linear_backward(c["G"], c["W"], c["X"], grad_x=outs.get("dgrad"),
+                                                           grad_w=outs.get("wgrad"))
+    elif not c["grouped"]:
         outs["dgrad"] = bsq.linear_dgrad(c["G"], c["W"], out=outs.get("dgrad"))
         outs["wgrad"] = bsq.linear_wgrad(c["G"], c["X"], out=outs.get("wgrad"))
     else:

@@ -69,3 +69,15 @@ def test_empty_problems_return_ok_without_launch(L):
     assert _dgrad(L, M=0) == bsq.BSQ_OK
     assert _dgrad(L, K=0) == bsq.BSQ_OK
     assert L.bsq_dequant(1, FAKE, FAKE, None, 0, 4, 32, FAKE, None) == bsq.BSQ_OK
+
+
+def test_linear_backward_validation(L):
+    def bw(needs, w=FAKE, x=FAKE, gx=FAKE, gw=FAKE, wf=1, xf=1):
+        return L.bsq_linear_backward(FAKE, 64, 128, wf, w, FAKE, None, xf, x, FAKE, None, 256, needs, gx, gw, None)
+    assert bw(0, w=None, x=None, gx=None, gw=None) == bsq.BSQ_OK          # nothing wanted: nothing read
+    assert bw(4) == bsq.BSQ_ERR_INVALID_ARG                               # unknown mask bit
+    assert bw(bsq.BSQ_NEEDS_GRAD_X, w=None) == bsq.BSQ_ERR_INVALID_ARG    # W needed for grad_x
+    assert bw(bsq.BSQ_NEEDS_GRAD_W, x=None) == bsq.BSQ_ERR_INVALID_ARG    # X needed for grad_w
+    assert bw(3, gw=None) == bsq.BSQ_ERR_INVALID_ARG
+    assert bw(3, xf=9) == bsq.BSQ_ERR_INVALID_ARG
+    assert "bsq_linear" in bsq.last_error()

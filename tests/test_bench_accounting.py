@@ -114,3 +114,14 @@ def test_single_process_and_job_throughput():
     assert bench.max_over_ranks(7.0) == 7.0           # no process group: unchanged
     # 2 replicas x 1 TFLOP per step x 10 steps in 20 ms -> 1000 TFLOP/s for the job
     assert bench.job_tflops(2, 1e12, 10, 20.0) == pytest.approx(1000.0)
+
+
+def test_fused_step_reads_grad_out_once():
+    """The fused backward launch of a linear workload moves both packed operands, grad_out
+    once and both outputs: MXFP4 4096^3 = 2 x (8.39 MB codes + 0.52 MB scales) + 3 x 33.55 MB."""
+    name, flops, nbytes = bench.step_plan(_cfg(2))
+    assert name == "backward"
+    assert flops / 1e9 == pytest.approx(274.878, abs=5e-3)
+    assert nbytes / MB == pytest.approx(118.489, abs=5e-3)
+    assert bench.step_plan(_cfg(1)) is None        # W E4M3, X BF16: two launches
+    assert bench.step_plan(_cfg(5)) is None        # grouped

@@ -9,8 +9,9 @@ float64 oracle on four columns of every 128-column block (every m-tile of every 
 then runs REPS more times into buffers refilled with NaN; every tile's accumulation order
 is fixed, so each repeat must equal the first run bit for bit over the whole output.
 
-Workloads: MXFP4 4096^3 dense dgrad and wgrad, and the 128-expert MXFP4 grouped dgrad
-and wgrad (Dirichlet(0.3) routing, empty experts; its wgrad takes the short-tile kernel).
+Workloads: MXFP4 4096^3 dense dgrad and wgrad, as one fused backward launch and as the two
+single-product launches, and the 128-expert MXFP4 grouped dgrad and wgrad (Dirichlet(0.3)
+routing, empty experts; its wgrad takes the short-tile kernel).
 """
 
 import pytest
@@ -32,16 +33,19 @@ def cfg(request):
     torch.cuda.empty_cache()
 
 
-def test_repeats_match_oracle_and_first_run(cfg):
+@pytest.mark.parametrize("fused", [True, False])
+def test_repeats_match_oracle_and_first_run(cfg, fused):
     c = cfg
-    first = run_config(c)
+    if c["grouped"] and not fused:
+        pytest.skip("the grouped workload has one launch per product either way")
+    first = run_config(c, fused=fused)
     check_config_sampled(c, first, block_cols(c["K"], 4, 7))
     ref = {k: v.clone() for k, v in first.items()}
     bad = []
     for rep in range(REPS):
         for v in first.values():
             v.fill_(float("nan"))
-        run_config(c, first)
+        run_config(c, first, fused=fused)
         for k, v in first.items():
             if not torch.equal(v.view(torch.int16), ref[k].view(torch.int16)):
                 diff = (v.view(torch.int16) != ref[k].view(torch.int16))
