@@ -49,7 +49,53 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the headline workload (not the other four, nor the standalone dequant)")
+    ap.add_argument("--profile", default=None,
+                    choices=["backward", "dgrad", "wgrad", "grouped_dgrad", "grouped_wgrad", "small_m", "dequant"],
+                    help="run only this op of the workload, --warmup + --steps times back to back, and print "
+                         "its mean time (a fixed launch sequence for ncu; not a benchmark line)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="grouped workloads: scale down to this many experts (same tokens per expert)")
     return ap.parse_args()
+
+
+def profile_run(args, bsq, synth, dev):
+    """--profile: one op of the workload, back to back (no L2 flush in between)."""
+    c = synth.make_config(args.config, device=dev, seed=0, experts=args.experts)
+    if c["grouped"]:
+        c["offsets_dev"] = torch.from_numpy(c["offsets"]).to(dev)
+    outs = alloc_outputs(c, dev)
+    op = args.profile
+    if op == "backward":
+        f = lambda: bsq.linear_backward(c["G"], c["W"], c["X"], grad_x=outs["dgrad"], grad_w=outs["wgrad"])
+    elif op == "dgrad":
+        f = lambda: bsq.linear_dgrad(c["G"], c["W"], out=outs["dgrad"])
+    elif op == "wgrad":
+        f = lambda: bsq.linear_wgrad(c["G"], c["X"], out=outs["wgrad"])
+    elif op == "grouped_dgrad":
+        f = lambda: bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=outs["grouped_dgrad"])
+    elif op == "grouped_wgrad":
+        f = lambda: bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=outs["grouped_wgrad"])
+    elif op == "small_m":
+        so = torch.empty((c["G_small"].shape[0], c["K"]), dtype=torch.bfloat16, device=dev)
+        f = lambda: bsq.linear_dgrad(c["G_small"], c["W"], out=so)
+    else:
+        do = torch.empty((c["W"].batch, c["W"].rows, c["W"].cols), dtype=torch.bfloat16, device=dev)
+        f = lambda: bsq.dequant(c["W"], out=do)
+    for _ in range(args.warmup):
+        f()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        f()
+    b.record()
+    torch.cuda.synchronize()
+    st, code = bsq.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error {code}")
+    print(json.dumps({"profile": op, "workload": c["name"], "launches": args.warmup + args.steps,
+                      "mean_ms": a.elapsed_time(b) / max(1, args.steps)}))
+    return 0
 
 
 # ---------------------------------------------------------------- work accounting
@@ -421,8 +467,14 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     for name, fl, nb in ops:
         ms = statistics.median(per_op[name])
         r["ops"][name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "roofline": op_roofline(fl, nb, ms, pk)}
+        r["ops"][name]["roofline"]["traffic"] = profiled_traffic(c["name"], name)
     ms = statistics.median(step_ms)
     fl = sum(o[1] for o in ops)
+    sp = step_plan(c)
+    if sp is not None:
+        r["backward"] = {"ms": ms, "tflops": sp[1] / (ms * 1e-3) / 1e12,
+                         "roofline": op_roofline(sp[1], sp[2], ms, pk)}
+        r["backward"]["roofline"]["traffic"] = profiled_traffic(c["name"], "backward")
     r["step_ms"] = ms
     r["tflops"] = fl / (ms * 1e-3) / 1e12
     r["frac_burst"] = r["tflops"] / pk["bf16_tflops"]
@@ -582,6 +634,8 @@ def main():
     torch.cuda.set_device(dev)
     from block_scaled_gemm_fp8_gb300 import bsq
     bsq.lib()
+    if args.profile:
+        return profile_run(args, bsq, synth, dev)
 
     c = synth.make_config(args.config, device=dev, seed=0)
     if c["grouped"]:

@@ -281,12 +281,14 @@ CONFIG_NAMES = {
 }
 
 
-def make_config(n, device="cpu", seed=0, small_m=16):
+def make_config(n, device="cpu", seed=0, small_m=16, experts=None):
     """Inputs of workload ``n`` (1..5) on ``device``; returns a dict of tensors and sizes.
 
     Keys: ``G`` (bf16 grad_out), ``W`` (Packed, [E or 1, N, K]), ``X`` (Packed or None,
     [1, M, K]), ``offsets`` (int32 numpy, grouped only), sizes M/S, N, K, E, and for
-    workload 2 ``G_small`` (bf16 [small_m, N]).
+    workload 2 ``G_small`` (bf16 [small_m, N]).  ``experts`` (grouped workloads only)
+    scales the workload down to that many experts with the same tokens per expert and
+    the same routing law (a smaller case of the same kernels, e.g. for profiling).
     """
     base = seed * 100
     if n == 1:
@@ -310,18 +312,24 @@ def make_config(n, device="cpu", seed=0, small_m=16):
         return dict(name=CONFIG_NAMES[n], M=M, N=N, K=K, E=1, G=G, W=W, X=X, grouped=False)
     if n == 4:
         E, S, N, K = 64, 16384, 2816, 2048
-        counts = zipf_counts(S, E, 1.1, base + 5)
+        if experts:
+            E, S = experts, S * experts // E
+        counts = zipf_counts(S, E, 1.1, base + 5, force_empty=[e for e in (0, 31, 63) if e < E])
         W = make_packed(FMT_FP8, E, N, K, 0.02, base + 2, device)
         G = randn((S, N), 1.0, base + 3, device, torch.bfloat16)
-        return dict(name=CONFIG_NAMES[n], M=S, N=N, K=K, E=E, G=G, W=W, X=None,
+        name = CONFIG_NAMES[n] if E == 64 else f"fp8_grouped_dgrad_E{E}_S{S}_N{N}_K{K}"
+        return dict(name=name, M=S, N=N, K=K, E=E, G=G, W=W, X=None,
                     offsets=offsets_from_counts(counts), grouped=True)
     if n == 5:
         E, S, N, K = 128, 32768, 2048, 7168
+        if experts:
+            E, S = experts, S * experts // E
         counts = dirichlet_counts(S, E, 0.3, base + 5)
         X = make_packed(FMT_MXFP4, 1, S, K, 1.0, base + 1, device)
         W = make_packed(FMT_MXFP4, E, N, K, 1.0, base + 2, device)
         G = randn((S, N), 1.0, base + 3, device, torch.bfloat16)
-        return dict(name=CONFIG_NAMES[n], M=S, N=N, K=K, E=E, G=G, W=W, X=X,
+        name = CONFIG_NAMES[n] if E == 128 else f"mxfp4_grouped_E{E}_S{S}_N{N}_K{K}"
+        return dict(name=name, M=S, N=N, K=K, E=E, G=G, W=W, X=X,
                     offsets=offsets_from_counts(counts), grouped=True)
     raise ValueError(n)
 
