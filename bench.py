@@ -76,6 +76,8 @@ def profile_run(args, bsq, synth, dev):
     elif op == "grouped_wgrad":
         f = lambda: bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=outs["grouped_wgrad"])
     elif op == "small_m":
+        if "G_small" not in c:
+            c["G_small"] = synth.randn((16, c["N"]), 1e-2, 7, dev, torch.bfloat16)
         so = torch.empty((c["G_small"].shape[0], c["K"]), dtype=torch.bfloat16, device=dev)
         f = lambda: bsq.linear_dgrad(c["G_small"], c["W"], out=so)
     else:
@@ -479,6 +481,13 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     r["tflops"] = fl / (ms * 1e-3) / 1e12
     r["frac_burst"] = r["tflops"] / pk["bf16_tflops"]
     r["frac_sustained"] = r["tflops"] / pk["bf16_tflops_sustained"]
+    if n in SMALL_M_WORKLOADS:
+        # M = 16 token rows against this workload's weight as well (the split-K kernel)
+        if "G_small" not in c:
+            c["G_small"] = synth.randn((16, c["N"]), 1e-2, 7, dev, torch.bfloat16)
+        ms, nbytes = time_small_m(c, bsq, steps, warmup, flush)
+        r["small_m_dgrad"] = {"M": 16, "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                              "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nbytes}
     deq = None
     if n in DEQUANT_WORKLOADS:
         deq = measure_dequant(c["W"], bsq, steps, warmup, flush, pk)
@@ -487,8 +496,10 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     return r, deq
 
 
-# The standalone dequant is timed on the packed weight of these workloads (one per format).
+# The standalone dequant is timed on the packed weight of these workloads (one per format);
+# the M = 16 dgrad on the headline weight and on these.
 DEQUANT_WORKLOADS = (3, 4, 5)
+SMALL_M_WORKLOADS = (3,)
 
 
 def measure_dequant(p, bsq, steps, warmup, flush, pk):

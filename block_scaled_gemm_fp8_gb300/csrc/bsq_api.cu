@@ -22,9 +22,6 @@ __device__ int32_t g_device_error;
 using bsq::kMaxDevices;
 int32_t* g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
-// Per-device FP32 workspace of the split-K small-M dgrad (zero between calls; grown on demand).
-void* g_ws[kMaxDevices] = {};
-size_t g_ws_bytes[kMaxDevices] = {};
 std::mutex g_mu;
 
 bsq_status fail(bsq_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -60,29 +57,6 @@ bsq_status device_state(int32_t** err, int* sms) {
   }
   *err = g_err_ptr[dev];
   *sms = g_num_sms[dev];
-  return BSQ_OK;
-}
-
-// Workspace of at least `need` bytes on the current device, zero-filled on the stream.
-bsq_status workspace(size_t need, cudaStream_t stream, void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ws_bytes[dev] < need) {
-    if (g_ws[dev]) {
-      cudaFree(g_ws[dev]);  // synchronizes the device: no kernel can still be using it
-      g_ws[dev] = nullptr;
-      g_ws_bytes[dev] = 0;
-    }
-    size_t bytes = need < (size_t(1) << 20) ? (size_t(1) << 20) : need;
-    e = cudaMalloc(&g_ws[dev], bytes);
-    if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "workspace cudaMalloc: %s", cudaGetErrorString(e));
-    e = cudaMemsetAsync(g_ws[dev], 0, bytes, stream);
-    if (e != cudaSuccess) return fail(BSQ_ERR_CUDA, "workspace memset: %s", cudaGetErrorString(e));
-    g_ws_bytes[dev] = bytes;
-  }
-  *out = g_ws[dev];
   return BSQ_OK;
 }
 
@@ -246,18 +220,16 @@ bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N, int32_t 
   if (M == 0 || K == 0) return BSQ_OK;
   if (N == 0) return zero_output(grad_x, M * K * 2, static_cast<cudaStream_t>(stream), what);
   if (M <= bsq::kSmallM && w_fmt != BSQ_BF16) {
-    // a few token rows: bound by reading W once; split-K kernel with an FP32 workspace
+    // a few token rows: bound by reading W once; split-K kernel whose row splits add up
+    // inside a thread-block cluster (no workspace)
     int32_t* err = nullptr;
     int sms = 0;
     st = device_state(&err, &sms);
     if (st != BSQ_OK) return st;
-    void* ws = nullptr;
-    st = workspace(bsq::smallm_workspace_bytes(K), static_cast<cudaStream_t>(stream), &ws);
-    if (st != BSQ_OK) return st;
-    bsq::SmallMArgs s{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, M, N, K, grad_x, ws, sms,
+    bsq::SmallMArgs s{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, M, N, K, grad_x, nullptr, sms,
                       static_cast<cudaStream_t>(stream), err};
     const char* msg = "";
-    if (bsq::launch_smallm(s, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
+    if (bsq::launch_smallm_cluster(s, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
     return BSQ_OK;
   }
   bsq::GemmArgs a{};

@@ -76,6 +76,9 @@ struct SmallMArgs {
 constexpr int kSmallM = 16;  // dgrad with at most this many rows takes the split-K kernel
 size_t smallm_workspace_bytes(int64_t K);
 int launch_smallm(const SmallMArgs& a, const char** msg);
+// The same product with the row splits of a column slab reduced inside a thread-block
+// cluster (distributed shared memory): no workspace (a.ws is not used).
+int launch_smallm_cluster(const SmallMArgs& a, const char** msg);
 
 // Host-side argument checks of bsq_linear_dgrad (bsq_api.cu); BSQ_OK when well formed.
 int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,

@@ -97,6 +97,12 @@ __device__ __forceinline__ void st_async_tx_rank(uint32_t dst, uint32_t bar, uin
                "r"(0u), "r"(map_to_rank(bar, rank))
                : "memory");
 }
+// 32-bit load from a shared::cluster address (another CTA's shared memory, via map_to_rank).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 // 32-bit store to the same offset in CTA `rank`.
 __device__ __forceinline__ void st_rank_u32(uint32_t addr, uint32_t rank, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_rank(addr, rank)), "r"(v) : "memory");

@@ -12,9 +12,12 @@
 //     (one byte permute + the multiply-spread of bsq_decode.cuh), which is exactly the
 //     k-pair an mma.sync B fragment wants, so no transpose and no BF16 staging is needed;
 //   * m16n8k16 BF16 mma.sync with FP32 accumulators (tokens are the M=16 side);
-//   * the warps of a CTA reduce through shared memory, the CTAs of a slab through an FP32
-//     workspace with 16-byte reduction atomics; the last CTA to finish a slab converts it
-//     to BF16, writes grad_X and zeroes the workspace again.
+//   * the warps of a CTA reduce through shared memory.  The row splits of a slab then add
+//     up in one of two ways: smallm_dgrad_cluster_kernel (bsq_linear_dgrad) makes them one
+//     thread-block cluster and adds through distributed shared memory; smallm_dgrad_kernel
+//     (the allocation-free entry point) adds into an FP32 scratch with 16-byte reduction
+//     atomics, and the last CTA of a slab converts it to BF16, writes grad_X and zeroes the
+//     scratch again.
 #include <cstdio>
 #include <mutex>
 
@@ -338,6 +341,314 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
   if (tid == 0) p.counters[slab] = 0;
 }
 
+// ---------------------------------------------------------------- cluster-reduced variant
+// The same product without any global workspace: the CTAs that split a column slab's rows
+// form one thread-block cluster and add their partial sums through distributed shared
+// memory.  Each CTA streams its rows in 64-row chunks, each chunk on its own barrier, so
+// decoding starts with the first chunk instead of after the whole slab.
+constexpr int kChunk = 64;        // rows of W per TMA chunk (four mma k-steps)
+constexpr int kRing = 8;          // chunks in flight per CTA
+constexpr int kMaxSplits = 8;     // CTAs of a cluster (portable cluster size)
+
+struct ClusterParams {
+  const uint8_t* scale;
+  const float* tensor_scale;
+  __nv_bfloat16* out;
+  int32_t M, N, K;
+  int32_t rows_per_split;   // multiple of kChunk
+  int32_t scale_ld;         // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128)
+  int32_t scale_tma;        // FP4 scale windows through TMA
+  uint64_t timeout_ns;
+  int32_t* err;
+};
+
+template <int FMT>
+struct ClusterFmt {
+  static constexpr int kRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2;
+  static constexpr int kWBytes = kChunk * kRowBytes;
+  static constexpr int kSBytes = FMT == BSQ_FP8_E4M3_B128 ? 0 : kChunk * 16;
+  static constexpr int kGBytes = 16 * kChunk * 2;   // [16 tokens][64 rows] BF16, 128-byte swizzled
+  static constexpr int kSlotBytes = kWBytes + kSBytes + kGBytes;
+  static_assert(kSlotBytes % 1024 == 0, "swizzled grad_out boxes need 1024-byte aligned slots");
+  static constexpr int kRingBytes = kRing * kSlotBytes;
+  static constexpr int kTreeBytes = kWarps * 16 * kSlab * 4;   // partials of the eight warps
+  static constexpr int kStaged = kRingBytes > kTreeBytes ? kRingBytes : kTreeBytes;
+  static constexpr int kRedBytes = 16 * kSlab * 4;        // this CTA's partial, read by the cluster
+  static constexpr int kSmem = kStaged + kRedBytes + 256 + 1024;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreadsSm, 2)
+    smallm_dgrad_cluster_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+                                const __grid_constant__ CUtensorMap tm_g, const ClusterParams p) {
+  using F = ClusterFmt<FMT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* tree = reinterpret_cast<float*>(base);                  // warp partials; reuse the ring after the last chunk
+  float* red = reinterpret_cast<float*>(base + F::kStaged);      // [16 tokens][128 columns]
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + F::kStaged + F::kRedBytes);
+  uint64_t* empty = full + kRing;
+  int32_t* fills = reinterpret_cast<int32_t*>(empty + kRing);   // copies issued into each slot
+  const int slab = blockIdx.x;
+  const int cb = slab * kSlab;
+  const int n0 = blockIdx.y * p.rows_per_split;
+  const int n1 = min(p.N, n0 + p.rows_per_split);
+  const int nchunks = n1 > n0 ? (n1 - n0 + kChunk - 1) / kChunk : 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int grp = warp >> 2;         // warps 0-3 take even chunks, 4-7 odd ones
+  const int kstep = warp & 3;        // the warp's 16-row k-step of a chunk
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t csize = gridDim.y;  // the cluster spans the row splits of one slab
+
+  auto slot_of = [&](int c) { return base + (c % kRing) * F::kSlotBytes; };
+  auto issue = [&](int c) {          // TMA of chunk c into its ring slot
+    uint8_t* s = slot_of(c);
+    fills[c % kRing] += 1;
+    const uint32_t bar = smem_u32(&full[c % kRing]);
+    const int row = n0 + c * kChunk;
+    mbar_arrive_expect_tx(bar, F::kWBytes + ((F::kSBytes && p.scale_tma) ? F::kSBytes : 0) + F::kGBytes);
+    tma_load_2d(smem_u32(s), &tm_w, bar, FMT == BSQ_FP8_E4M3_B128 ? cb : cb / 2, row);
+    if (F::kSBytes && p.scale_tma)
+      tma_load_2d(smem_u32(s + F::kWBytes), &tm_s, bar, (FMT == BSQ_MXFP4 ? (cb >> 5) : (cb >> 4)) & ~15, row);
+    tma_load_2d(smem_u32(s + F::kWBytes + F::kSBytes), &tm_g, bar, row, 0);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 4);   // the four warps of the chunk's group
+      fills[s] = 0;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int c = 0; c < min(nchunks, kRing); ++c) issue(c);
+
+  float tscale = 0.f;
+  if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale);
+  const int col = cb + 16 * g;
+  const bool col_ok = col < p.K;
+  float acc[kNT][4];
+#pragma unroll
+  for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  bool ok = true;
+  for (int c = grp; c < nchunks; c += 2) {
+    const int si = c % kRing;
+    const uint32_t par = (c / kRing) & 1u;
+    {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait_sleep(smem_u32(&full[si]), par, 20000u)) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    const uint8_t* ws_w = slot_of(c);
+    const uint8_t* ws_s = ws_w + F::kWBytes;
+    const uint32_t gb = smem_u32(ws_w + F::kWBytes + F::kSBytes);
+    const int lr = kstep * kStep;                 // the k-step's first row inside the chunk
+    const int grow0 = n0 + c * kChunk + lr;       // its row of W
+    const int rows[4] = {lr + 2 * q, lr + 2 * q + 1, lr + 8 + 2 * q, lr + 9 + 2 * q};
+    // A fragment: grad_out[token][k], k = the k-step's 16 rows (chunk lr/8, lr/8 + 1 of the
+    // 128-byte swizzled [16 tokens][64 rows] box)
+    const uint32_t c0 = static_cast<uint32_t>(((lr >> 3) ^ (g & 7)) << 4);
+    const uint32_t c1 = static_cast<uint32_t>((((lr >> 3) + 1) ^ (g & 7)) << 4);
+    uint32_t a[4];
+    a[0] = lds_u32(gb + g * 128 + c0 + 4 * q);
+    a[1] = lds_u32(gb + (g + 8) * 128 + c0 + 4 * q);
+    a[2] = lds_u32(gb + g * 128 + c1 + 4 * q);
+    a[3] = lds_u32(gb + (g + 8) * 128 + c1 + 4 * q);
+    if (FMT == BSQ_FP8_E4M3_B128) {
+      float sf = 0.f;
+      if (col_ok && grow0 < n1)
+        sf = __ldg(reinterpret_cast<const float*>(p.scale) + static_cast<int64_t>(grow0 >> 7) * p.scale_ld + (col >> 7));
+      const ScaleBf16 sc = make_scale_fp8(sf);   // one 128-row block holds the whole k-step
+      uint4 w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(ws_w + rows[i] * F::kRowBytes + 16 * g);
+      const bool any_nan = e4m3_any_nan(w[0].x | w[0].y | w[0].z | w[0].w | w[1].x | w[1].y | w[1].z | w[1].w |
+                                        w[2].x | w[2].y | w[2].z | w[2].w | w[3].x | w[3].y | w[3].z | w[3].w);
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        uint32_t b0[4], b1[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+          const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+          uint32_t(&dst)[4] = half ? b1 : b0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // byte j of both rows, each in the low byte of its 16-bit half with a sign-filled
+            // byte above it; a 4-bit shift puts the magnitude bits on BF16 bits 10..4 and the
+            // sign on bit 15 (code value x 2^-120)
+            const uint32_t v = prmt(xw[wi], yw[wi], static_cast<uint32_t>(j | ((j | 8) << 4) | ((4 + j) << 8) |
+                                                                              (((4 + j) | 8) << 12)));
+            dst[j] = (v << 4) & 0x87F087F0u;
+          }
+        }
+        if (sc.fast) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            b0[j] = bf16x2_mul(b0[j], sc.c2);
+            b1[j] = bf16x2_mul(b1[j], sc.c2);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            b0[j] = bf16x2_mul(bf16x2_mul(b0[j], kPow2_120x2), sc.s2);
+            b1[j] = bf16x2_mul(bf16x2_mul(b1[j], kPow2_120x2), sc.s2);
+          }
+        }
+        if (any_nan) {
+          // S.1111.111 is NaN in E4M3; the bit move above does not see it
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+            const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+            uint32_t(&dst)[4] = half ? b1 : b0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (((xw[wi] >> (8 * j)) & 0x7Fu) == 0x7Fu) dst[j] = (dst[j] & 0xFFFF0000u) | kBf16NaN;
+              if (((yw[wi] >> (8 * j)) & 0x7Fu) == 0x7Fu) dst[j] = (dst[j] & 0xFFFFu) | (kBf16NaN << 16);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_bf16_16816(acc[4 * wi + j], a, b0[j], b1[j]);
+      }
+    } else {
+      uint2 w[4];
+      uint32_t sraw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[i] = *reinterpret_cast<const uint2*>(ws_w + rows[i] * F::kRowBytes + 8 * g);
+        const int grow = n0 + c * kChunk + rows[i];
+        if (p.scale_tma) {
+          sraw[i] = FMT == BSQ_MXFP4 ? ws_s[rows[i] * 16 + ((cb >> 5) & 15) + (g >> 1)]
+                                     : ws_s[rows[i] * 16 + ((cb >> 4) & 15) + g];
+        } else {
+          sraw[i] = 0;
+          if (col_ok && grow < n1)
+            sraw[i] = __ldg(p.scale + static_cast<int64_t>(grow) * p.scale_ld + (FMT == BSQ_MXFP4 ? (col >> 5) : (col >> 4)));
+        }
+      }
+      // the scales of the k-step's four rows (rows 2q, 2q+1 pair in b0, rows 8+2q, 9+2q in b1)
+      const ScaleBf16 sc0 = pair_scales(row_scale<FMT>(sraw[0], tscale), row_scale<FMT>(sraw[1], tscale));
+      const ScaleBf16 sc1 = pair_scales(row_scale<FMT>(sraw[2], tscale), row_scale<FMT>(sraw[3], tscale));
+      const bool fast = sc0.fast && sc1.fast;
+#pragma unroll
+      for (int wi = 0; wi < 2; ++wi) {
+        uint32_t b0[8], b1[8];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+          const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+          uint32_t(&dst)[8] = half ? b1 : b0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t v = pair_bytes(xw[wi], yw[wi], j);                // byte 4wi+j of both rows
+            dst[2 * j] = ((v & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;         // column 8wi+2j
+            dst[2 * j + 1] = ((v & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;     // column 8wi+2j+1
+          }
+        }
+        if (fast) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            b0[j] = bf16x2_mul(b0[j], sc0.c2);
+            b1[j] = bf16x2_mul(b1[j], sc1.c2);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            b0[j] = scale_one(b0[j], sc0, kPow2_126x2);
+            b1[j] = scale_one(b1[j], sc1, kPow2_126x2);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mma_bf16_16816(acc[8 * wi + j], a, b0[j], b1[j]);
+      }
+    }
+    // this warp is done with the chunk's slot; the group's first warp refills it with the
+    // chunk kRing later once all four have let it go
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[si]));
+    if (kstep == 0 && lane == 0 && c + kRing < nchunks) {
+      const uint64_t t0 = global_timer_ns();
+      bool freed = true;
+      while (!mbar_try_wait(smem_u32(&empty[si]), par)) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          freed = false;
+          break;
+        }
+      }
+      if (freed) issue(c + kRing);
+      else ok = false;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+  }
+  // One decision for the CTA; after a timeout the CTA writes nothing but still meets its
+  // cluster at both barriers (its peers read its partial, which is then undefined).
+  ok = __syncthreads_and(ok) != 0;
+  if (!ok) {
+    if (tid == 0) {
+      atomicCAS(p.err, 0, BSQ_DEVERR_TIMEOUT);
+      // let the copies still in flight land before the shared memory is reused or freed:
+      // the last fill of every slot (slot fills are issued in order)
+      for (int s = 0; s < kRing; ++s) {
+        if (fills[s] == 0) continue;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&full[s]), (fills[s] - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+        }
+      }
+    }
+    __syncthreads();
+  } else {
+    // Every warp stores its partial through the idle ring, fragment by fragment
+    // ([warp][n-tile][fragment register][lane], conflict-free); then every thread adds the
+    // eight warps' values of its entries and writes the CTA's partial red[token][column]
+    // (column = 16 n + n-tile of the slab).
+    {
+      float* dst = tree + warp * (kNT * 4 * 32);
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) dst[(nt * 4 + r) * 32 + lane] = acc[nt][r];
+    }
+    __syncthreads();
+    for (int e = tid; e < kNT * 4 * 32; e += kThreadsSm) {
+      float v = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) v += tree[w2 * (kNT * 4 * 32) + e];
+      const int l = e & 31, rr = (e >> 5) & 3, nt = e >> 7;
+      const int t = (l >> 2) + ((rr & 2) ? 8 : 0), n = 2 * (l & 3) + (rr & 1);
+      red[t * kSlab + 16 * n + nt] = v;
+    }
+  }
+  // Every partial of the cluster is in place (release/acquire at cluster scope) ...
+  cluster_sync();
+  // ... and CTA r of the cluster adds columns [r*cw, (r+1)*cw) of the slab over all of them.
+  const int cw = ((kSlab + static_cast<int>(csize) - 1) / static_cast<int>(csize) + 3) & ~3;
+  const int c_lo = static_cast<int>(crank) * cw, c_hi = min(kSlab, c_lo + cw);
+  if (ok && c_hi > c_lo) {
+    const int span = c_hi - c_lo;
+    for (int i = tid; i < p.M * span; i += kThreadsSm) {
+      const int t = i / span, cc = c_lo + i % span;
+      const uint32_t off = smem_u32(red + t * kSlab + cc);
+      float v = 0.f;
+      for (uint32_t r = 0; r < csize; ++r) v += ld_shared_cluster_f32(map_to_rank(off, r));
+      if (cb + cc < p.K) p.out[static_cast<int64_t>(t) * p.K + cb + cc] = __float2bfloat16_rn(v);
+    }
+  }
+  // No CTA leaves while its peers may still read its partial.
+  cluster_sync();
+}
+
 }  // namespace
 
 size_t smallm_workspace_bytes(int64_t K) {
@@ -434,15 +745,110 @@ int launch_smallm(const SmallMArgs& a, const char** msg) {
   return 0;
 }
 
+int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
+  ClusterParams p;
+  p.scale = static_cast<const uint8_t*>(a.w_scale);
+  p.tensor_scale = a.w_tensor_scale;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.K = static_cast<int32_t>(a.K);
+  p.err = a.err;
+  p.timeout_ns = wait_limit_ns();
+  p.scale_ld = a.fmt == BSQ_MXFP4 ? static_cast<int32_t>(a.K / 32)
+               : a.fmt == BSQ_NVFP4 ? static_cast<int32_t>(a.K / 16)
+                                    : static_cast<int32_t>((a.K + 127) / 128);
+  const int slabs = static_cast<int>((a.K + kSlab - 1) / kSlab);
+  // Row splits = the cluster size: about two CTAs per SM in one wave, at most 8, and no
+  // more splits than 64-row chunks.
+  int splits = (2 * a.num_sms) / slabs;
+  const int64_t max_by_rows = (a.N + kChunk - 1) / kChunk;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits > max_by_rows) splits = static_cast<int>(max_by_rows);
+  if (splits < 1) splits = 1;
+  int64_t rps = (a.N + splits - 1) / splits;
+  rps = (rps + kChunk - 1) / kChunk * kChunk;
+  p.rows_per_split = static_cast<int32_t>(rps);
+  CUtensorMap tm_w, tm_s, tm_g;
+  const uint64_t wrow = a.fmt == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
+  {
+    const uint64_t dims[2] = {wrow, static_cast<uint64_t>(a.N)};
+    const uint64_t strides[1] = {wrow};
+    const uint32_t box[2] = {static_cast<uint32_t>(a.fmt == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2),
+                             static_cast<uint32_t>(kChunk)};
+    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      *msg = "tensor map encoding failed for W";
+      return -1;
+    }
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {64, 16};
+    if (!encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
+      *msg = "tensor map encoding failed for grad_out";
+      return -1;
+    }
+  }
+  tm_s = tm_w;
+  p.scale_tma = 0;
+  if (a.fmt == BSQ_MXFP4 || a.fmt == BSQ_NVFP4) {
+    const uint64_t srow = a.fmt == BSQ_MXFP4 ? a.K / 32 : a.K / 16;
+    if (srow % 16 == 0 && (reinterpret_cast<uintptr_t>(a.w_scale) & 15u) == 0) {
+      const uint64_t dims[2] = {srow, static_cast<uint64_t>(a.N)};
+      const uint64_t strides[1] = {srow};
+      const uint32_t box[2] = {16, static_cast<uint32_t>(kChunk)};
+      if (!encode_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_scale, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        *msg = "tensor map encoding failed for the scales";
+        return -1;
+      }
+      p.scale_tma = 1;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(splits));
+  cfg.blockDim = dim3(kThreadsSm);
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaSuccess;
+#define BSQ_LAUNCH_CLUSTER(F_)                                                                                       \
+  cfg.dynamicSmemBytes = ClusterFmt<F_>::kSmem;                                                                     \
+  e = cudaFuncSetAttribute(smallm_dgrad_cluster_kernel<F_>, cudaFuncAttributeMaxDynamicSharedMemorySize,           \
+                           ClusterFmt<F_>::kSmem);                                                                  \
+  if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, smallm_dgrad_cluster_kernel<F_>, tm_w, tm_s, tm_g, p);
+  switch (a.fmt) {
+    case BSQ_MXFP4: BSQ_LAUNCH_CLUSTER(BSQ_MXFP4) break;
+    case BSQ_NVFP4: BSQ_LAUNCH_CLUSTER(BSQ_NVFP4) break;
+    case BSQ_FP8_E4M3_B128: BSQ_LAUNCH_CLUSTER(BSQ_FP8_E4M3_B128) break;
+    default:
+      *msg = "small-M dgrad: unsupported format";
+      return -1;
+  }
+#undef BSQ_LAUNCH_CLUSTER
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *msg = cudaGetErrorString(e);
+    return static_cast<int>(e);
+  }
+  return 0;
+}
+
 }  // namespace bsq
 
 // ---------------------------------------------------------------- allocation-free entry point
 // Some callers cannot call cudaMalloc at all: code running inside a CUDA graph that is being
 // captured, allocators that own every byte of device memory, or hosts that forbid device
-// allocation after start-up.  bsq_linear_dgrad_smallm_noalloc serves them with the small-M
-// kernel above, its split-K scratch living in this file-scope device array instead of the
-// lazily allocated workspace.  The array exists on every device that loads the library,
-// for the life of the process.
+// allocation after start-up.  bsq_linear_dgrad_smallm_noalloc serves them with the
+// split-K small-M kernel above (smallm_dgrad_kernel), its scratch living in this
+// file-scope device array.  The array exists on every device that loads the library, for
+// the life of the process.
 namespace {
 
 constexpr int64_t kStaticMaxK = 16384;  // largest K the static scratch serves

@@ -42,11 +42,9 @@
  *     (an alignment above, too many experts); BSQ_ERR_CUDA a failed launch.
  *     Device-side conditions (decreasing offsets, a pipeline wait that ran out of
  *     time) are recorded in a per-device error word read by bsq_get_device_error.
- *   - Allocation: the caller owns every tensor.  The library's own device memory is one
- *     error word per device and, for bsq_linear_dgrad with M <= 16, one FP32 split-K
- *     workspace per device (16*K*4 bytes plus counters, at least 1 MiB) that the first such
- *     call allocates and a later call with a larger K re-allocates; make the first small-M
- *     call before any stream capture.  bsq_linear_dgrad_smallm_noalloc allocates nothing.
+ *   - Allocation: the caller owns every tensor.  The library allocates no device memory:
+ *     its own device state is one error word per device and the split-K scratch of
+ *     bsq_linear_dgrad_smallm_noalloc, both file-scope device arrays of the library.
  *   - Environment (read by the host side at every call; none changes a result beyond FP32
  *     summation order):
  *       BSQ_WAIT_LIMIT_US,    bound of every pipeline wait inside a kernel, in microseconds
@@ -100,8 +98,9 @@ bsq_status bsq_dequant(int32_t fmt, const void* data, const void* scale, const f
  * bsq_linear_dgrad -- grad_x[M][K] = grad_out[M][N] @ deq(W)[N][K]
  * (MSLK PR #393, Implementation Method; transformers PR #50031 FP8LinearFunction.backward).
  * grad_out: bf16[M][N]; W: packed [1][N][K] in w_fmt; grad_x: bf16[M][K] (fully written).
- * M <= 16 with a packed W takes a split-K kernel whose partial sums meet in the per-device
- * workspace: such calls on one device must not overlap in time (different streams).
+ * M <= 16 with a packed W takes a split-K kernel whose row splits add their partial sums
+ * inside a thread-block cluster (distributed shared memory): no workspace, so such calls
+ * may run concurrently on different streams.
  */
 bsq_status bsq_linear_dgrad(const void* grad_out, int64_t M, int64_t N,
                             int32_t w_fmt, const void* w_data, const void* w_scale,
@@ -173,9 +172,9 @@ bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N,
  * cannot allocate device memory (code running under stream capture, hosts whose allocator
  * owns all device memory, or processes that forbid allocation after start-up).  The pages
  * have no counterpart: it is an allocation-free variant of this library's split-K small-M
- * dgrad kernel.  Its FP32 split-K scratch is a file-scope device array of the library, not
- * the lazily allocated workspace bsq_linear_dgrad uses; every device that loads the library
- * holds that array (about 1 MiB) until the process exits.
+ * dgrad kernel that adds its row splits through global memory.  Its FP32 split-K scratch
+ * is a file-scope device array of the library; every device that loads the library holds
+ * that array (about 1 MiB) until the process exits.
  * Limits: 1 <= M <= 16, w_fmt FP8 / MXFP4 / NVFP4, K <= 16384; anything else returns
  * BSQ_ERR_UNSUPPORTED (or the usual argument errors) without launching.
  * Allocation: calls no cudaMalloc / cudaFree or any allocating routine.  The first call on
