@@ -26,7 +26,8 @@
 //   warp 2      allocates / frees TMEM; one lane relays "operand ready" to the even CTA
 //   warp 3      TMA producer of the grad_out ring: this CTA's half of the unit's tiles
 //   warp 1      MMA issuer, one thread of the even CTA: 4 x (256 x Nm x 16) per k-block
-//   warps 4-7   epilogue: tcgen05.ld -> BF16 -> global, one TMEM lane quarter each
+//   warps 4-7   epilogue: tcgen05.ld (pipelined, 16 columns at a time) -> BF16 -> global,
+//               one TMEM lane quarter each
 //   warps 8-23  dequantization, two teams of 8 warps; team t takes k-block t of every
 //               unit: packed codes (smem) -> BF16, written in the 128-byte swizzled
 //               MN-major layout the tensor core reads; also zero the rows of a k-block
@@ -645,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 4 + R::kEpiWarps) {
     // ===== epilogue =====
     // Warp w reads TMEM lane quarter w % 4; the kEpiPerQuarter warps of a quarter take its
-    // 32-column chunks in turn.
+    // 16-column chunks in turn.
     const int q = warp & 3;                   // TMEM lane quarter
     const int sub = R::kEpiPerQuarter > 1 ? (warp - 4) >> 2 : 0;   // 0 .. kEpiPerQuarter-1
     const int i = q * 32 + lane;              // accumulator row = tile m index (permuted)
@@ -677,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int nchunks = (ti.n_valid + 31) >> 5;
+      const int nchunks = (ti.n_valid + 15) >> 4;   // 16-column chunks of the accumulator
       // The even CTA's MMA thread reuses the accumulator once every epilogue warp of both
       // CTAs has released it: an even warp arrives expecting 4 bytes, an odd warp delivers
       // 4 bytes with an st.async (a cluster-scope release).
@@ -689,17 +690,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           else st_async_tx_rank(smem_u32(&sh.sink), smem_u32(&sh.tmem_empty[buf]), 0);
         }
       };
-      if (sub >= nchunks) release_acc();   // no chunk for this warp: release at once
+      if (sub >= nchunks) {
+        release_acc();   // no chunk for this warp: release at once
+        continue;
+      }
+      // The chunks of this warp, pipelined: once a chunk's TMEM load has landed it is packed
+      // to BF16 pairs, the next chunk's load is issued, and the packed chunk is stored while
+      // that load is in flight.
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN;
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(trow + sub * 16, v);
       for (int c = sub; c < nchunks; c += R::kEpiPerQuarter) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + c * 32, v);
         tmem_wait_ld();
-        if (c + R::kEpiPerQuarter >= nchunks) release_acc();
-        if (mok) {
-          const int nlim = min(32, ti.n_valid - c * 32);
+        uint32_t h[8];   // (n, n+1) pairs of this thread's column m, BF16
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nlim) obase[static_cast<int64_t>(c * 32 + j) * p.Kc] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        for (int j = 0; j < 8; ++j) h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        if (c + R::kEpiPerQuarter < nchunks) tmem_ld_32x32b_x16(trow + (c + R::kEpiPerQuarter) * 16, v);
+        else release_acc();   // every TMEM read of this warp has completed
+        if (mok) {
+          const int nlim = min(16, ti.n_valid - c * 16);
+          const int64_t step = p.Kc;
+          unsigned short* o = reinterpret_cast<unsigned short*>(obase) + static_cast<int64_t>(c * 16) * step;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j < nlim) *o = static_cast<unsigned short>((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
+            o += step;
+          }
         }
       }
     }
