@@ -31,7 +31,9 @@ FMT_BF16 = 0
 FMT_FP8 = 1
 FMT_MXFP4 = 2
 FMT_NVFP4 = 3
-FMT_NAMES = {FMT_BF16: "bf16", FMT_FP8: "fp8_e4m3_b128", FMT_MXFP4: "mxfp4", FMT_NVFP4: "nvfp4"}
+FMT_FP8_TENSOR = 4
+FMT_NAMES = {FMT_BF16: "bf16", FMT_FP8: "fp8_e4m3_b128", FMT_MXFP4: "mxfp4", FMT_NVFP4: "nvfp4",
+             FMT_FP8_TENSOR: "fp8_e4m3_tensor"}
 
 
 def _gen(device, seed):
@@ -80,6 +82,16 @@ def quantize_fp8_b128(w):
     q = (blocks / scale_inv[:, :, None, :, None]).clamp(-448.0, 448.0)
     codes = q.to(torch.float8_e4m3fn).view(torch.uint8).reshape(B, Rb * 128, Cb * 128)[:, :R, :C]
     return codes.contiguous(), scale_inv.contiguous()
+
+
+def quantize_fp8_tensor(w):
+    """float32 [B,R,C] -> (E4M3 codes uint8 [B,R,C], scale_inv float32 [B]): one scale per
+    batch entry (amax / 448; an all-zero entry gets 1)."""
+    B = w.shape[0]
+    amax = w.abs().reshape(B, -1).amax(dim=1)
+    scale_inv = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (w / scale_inv[:, None, None]).clamp(-448.0, 448.0)
+    return q.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), scale_inv.to(torch.float32).contiguous()
 
 
 def quantize_mxfp4(x):
@@ -146,6 +158,9 @@ def quantize(fmt, x):
     if fmt == FMT_FP8:
         d, s = quantize_fp8_b128(x)
         return Packed(fmt, d, s, None, B, R, C)
+    if fmt == FMT_FP8_TENSOR:
+        d, s = quantize_fp8_tensor(x)
+        return Packed(fmt, d, s, None, B, R, C)
     if fmt == FMT_MXFP4:
         d, s = quantize_mxfp4(x)
         return Packed(fmt, d, s, None, B, R, C)
@@ -181,13 +196,14 @@ def random_codes(fmt, batch, rows, cols, seed, device="cpu", scale_kind="random"
     replaced by 448 so that every decoded value is finite).
     """
     g = _gen(device, seed)
-    nbytes = cols if fmt == FMT_FP8 else cols // 2
+    fp8 = fmt in (FMT_FP8, FMT_FP8_TENSOR)
+    nbytes = cols if fp8 else cols // 2
     data = torch.randint(0, 256, (batch, rows, nbytes), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
-    if fmt == FMT_FP8 and scale_kind == "finite":
+    if fp8 and scale_kind == "finite":
         data = torch.where((data & 0x7F) == 0x7F, data - 1, data)   # S.1111.111 (NaN) -> S.1111.110 (448)
     ts = None
-    if fmt == FMT_FP8:
-        shape = (batch, -(-rows // 128), -(-cols // 128))
+    if fp8:
+        shape = (batch, -(-rows // 128), -(-cols // 128)) if fmt == FMT_FP8 else (batch,)
         s = torch.rand(shape, generator=g, device=device) + 0.5
         if scale_kind == "finite":
             # |code| <= 448 and scale < 2^117 keep every product below the BF16 maximum

@@ -9,6 +9,10 @@ significant bits and a BF16 scale at most 8) and rounded once, to nearest even.
     `_dequantize_fp8_weight` -- the scale grid is cast to the gradient dtype,
     repeated 128x along both axes, cropped to the weight's shape, and multiplied
     into the weight cast to that dtype.
+  * FP8 E4M3 with one float32 ``scale_inv`` per tensor: the same function's
+    `block_size is None` branch -- the scale, cast to the gradient dtype, is
+    broadcast over the weight without repetition; for a grouped weight [E, N, K]
+    there is one scale per expert.
   * MXFP4 (E2M1 codes, two per byte, one E8M0 scale per 32 consecutive elements
     of a row) and NVFP4 (E2M1 codes, one E4M3 scale per 16 consecutive elements
     of a row, one float32 scale per tensor): MSLK PR #393, "Implementation
@@ -31,6 +35,7 @@ from .formats import (E2M1_TABLE, E4M3_TABLE, E8M0_TABLE, bf16_bits, bf16_round,
 
 FMT_BF16 = "bf16"
 FMT_FP8 = "fp8_e4m3_b128"
+FMT_FP8_TENSOR = "fp8_e4m3_tensor"
 FMT_MXFP4 = "mxfp4"
 FMT_NVFP4 = "nvfp4"
 
@@ -56,6 +61,9 @@ def scale_values(fmt, scale, tensor_scale, batch, rows, cols):
         ri = np.arange(rows) // FP8_BLOCK
         ci = np.arange(cols) // FP8_BLOCK
         return s[:, ri][:, :, ci]
+    if fmt == FMT_FP8_TENSOR:
+        s = np.asarray(scale, dtype=np.float32).astype(np.float64).reshape(batch, 1, 1)
+        return np.broadcast_to(s, (batch, rows, cols))
     if fmt == FMT_MXFP4:
         b = np.asarray(scale, dtype=np.uint8).reshape(batch, rows, cols // MX_BLOCK)
         s = E8M0_TABLE[b]
@@ -73,7 +81,7 @@ def code_values(fmt, data, batch, rows, cols):
     if fmt == FMT_BF16:
         bits = np.asarray(data, dtype=np.uint16).reshape(batch, rows, cols)
         return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    if fmt == FMT_FP8:
+    if fmt in (FMT_FP8, FMT_FP8_TENSOR):
         return E4M3_TABLE[np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)]
     if fmt in (FMT_MXFP4, FMT_NVFP4):
         packed = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols // 2)
@@ -112,6 +120,10 @@ def dequant_cols(fmt, data, scale, tensor_scale, rows, cols, col_idx, batch_idx=
         s = np.asarray(scale, dtype=np.float32).astype(np.float64)
         s = s.reshape(batch, -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK))[batch_idx]
         s = s[np.arange(rows) // FP8_BLOCK][:, col_idx // FP8_BLOCK]
+    elif fmt == FMT_FP8_TENSOR:
+        codes = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)[batch_idx][:, col_idx]
+        v = E4M3_TABLE[codes]
+        s = float(np.asarray(scale, dtype=np.float32).reshape(batch)[batch_idx])
     else:
         packed = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols // 2)[batch_idx]
         byte = packed[:, col_idx // 2]
@@ -139,6 +151,10 @@ def dequant_rows(fmt, data, scale, tensor_scale, rows, cols, row_idx, batch_idx=
         s = np.asarray(scale, dtype=np.float32).astype(np.float64)
         s = s.reshape(batch, -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK))[batch_idx]
         s = s[row_idx // FP8_BLOCK][:, np.arange(cols) // FP8_BLOCK]
+    elif fmt == FMT_FP8_TENSOR:
+        codes = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)[batch_idx][row_idx]
+        v = E4M3_TABLE[codes]
+        s = float(np.asarray(scale, dtype=np.float32).reshape(batch)[batch_idx])
     else:
         packed = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols // 2)[batch_idx][row_idx]
         v = E2M1_TABLE[unpack_fp4(packed, cols)]

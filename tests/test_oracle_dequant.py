@@ -40,6 +40,41 @@ def _torch_fp8_dequant(codes_u8, scale_inv, rows, cols):
     return w * s
 
 
+def _torch_fp8_tensor_dequant(codes_u8, scale_inv):
+    """The page's recipe with block_size None, with torch ops: the scale cast to BF16 and
+    broadcast (one per batch entry), the weight cast to BF16, product rounded to BF16."""
+    w = torch.from_numpy(codes_u8).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    s = torch.from_numpy(np.asarray(scale_inv, dtype=np.float32)).to(torch.bfloat16)
+    return w * s.reshape(-1, *([1] * (w.dim() - 1)))
+
+
+@pytest.mark.parametrize("kind", ["random", "edge", "nan", "finite"])
+def test_fp8_per_tensor_scale_matches_page_recipe(kind):
+    """transformers PR #50031 `_dequantize_fp8_weight`, `block_size is None`: every code of a
+    three-expert weight against the torch restatement of that branch."""
+    p = synth.random_codes(synth.FMT_FP8_TENSOR, 3, 130, 96, seed=21, scale_kind=kind)
+    d, s, _ = p.numpy()
+    got = D.dequant_bits(D.FMT_FP8_TENSOR, d, s, None, 3, 130, 96)
+    assert _same_bits(got, _torch_bits(_torch_fp8_tensor_dequant(d, s)))
+    cols, rows = np.array([0, 17, 95]), np.array([0, 64, 129])
+    full = D.dequant_values(D.FMT_FP8_TENSOR, d, s, None, 3, 130, 96)
+    for b in range(3):
+        np.testing.assert_array_equal(D.dequant_cols(D.FMT_FP8_TENSOR, d, s, None, 130, 96, cols, b, 3),
+                                      full[b][:, cols])
+        np.testing.assert_array_equal(D.dequant_rows(D.FMT_FP8_TENSOR, d, s, None, 130, 96, rows, b, 3),
+                                      full[b][rows])
+
+
+def test_fp8_per_tensor_scale_is_a_constant_block_grid():
+    """One scale per tensor decodes exactly as 128x128 blocks that all hold that scale."""
+    p = synth.random_codes(synth.FMT_FP8_TENSOR, 2, 300, 256, seed=22)
+    d, s, _ = p.numpy()
+    grid = np.repeat(s.reshape(2, 1, 1), 3, axis=1).repeat(2, axis=2).astype(np.float32)
+    a = D.dequant_bits(D.FMT_FP8_TENSOR, d, s, None, 2, 300, 256)
+    b = D.dequant_bits(D.FMT_FP8, d, grid, None, 2, 300, 256)
+    assert _same_bits(a, b)
+
+
 def test_fp8_linear_example_shape_from_page():
     ex = GOLDEN["fp8_linear_example"]
     N, K = ex["out_features"], ex["in_features"]

@@ -71,3 +71,15 @@ def test_grouped_off_by_one_is_caught(monkeypatch):
         return r0, int(offsets[e])
     monkeypatch.setattr(Gm, "expert_rows", shifted)
     assert _fails(TG.test_grouped_dgrad_equals_block_diagonal_dense)
+
+
+def test_per_tensor_scale_of_the_wrong_expert_is_caught(monkeypatch):
+    real = D.scale_values
+
+    def first_expert_only(fmt, scale, tensor_scale, batch, rows, cols):
+        if fmt == D.FMT_FP8_TENSOR:
+            s = np.asarray(scale, dtype=np.float32).astype(np.float64).reshape(batch)
+            return np.broadcast_to(np.full((batch, 1, 1), s[0]), (batch, rows, cols))
+        return real(fmt, scale, tensor_scale, batch, rows, cols)
+    monkeypatch.setattr(D, "scale_values", first_expert_only)
+    assert _fails(TD.test_fp8_per_tensor_scale_matches_page_recipe, "random")
