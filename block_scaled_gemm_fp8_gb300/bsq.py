@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libbsq.so")
 HEADER_PATH = os.path.join(HERE, "..", "include", "bsq.h")
 
-BSQ_BF16, BSQ_FP8_E4M3_B128, BSQ_MXFP4, BSQ_NVFP4 = 0, 1, 2, 3
+BSQ_BF16, BSQ_FP8_E4M3_B128, BSQ_MXFP4, BSQ_NVFP4, BSQ_FP8_E4M3_TENSOR = 0, 1, 2, 3, 4
 BSQ_OK, BSQ_ERR_INVALID_ARG, BSQ_ERR_UNSUPPORTED, BSQ_ERR_CUDA, BSQ_ERR_TIMEOUT = 0, 1, 2, 3, 4
 BSQ_NEEDS_GRAD_X, BSQ_NEEDS_GRAD_W = 1, 2
 

@@ -65,7 +65,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Shared validation of a packed operand [batch][rows][cols].
 bsq_status check_packed(const char* what, int32_t fmt, const void* data, const void* scale, const float* ts,
                         int64_t batch, int64_t rows, int64_t cols, bool allow_bf16) {
-  if (fmt < BSQ_BF16 || fmt > BSQ_NVFP4) return fail(BSQ_ERR_INVALID_ARG, "%s: unknown format %d", what, fmt);
+  if (fmt < BSQ_BF16 || fmt > BSQ_FP8_E4M3_TENSOR) return fail(BSQ_ERR_INVALID_ARG, "%s: unknown format %d", what, fmt);
   if (fmt == BSQ_BF16 && !allow_bf16) return fail(BSQ_ERR_UNSUPPORTED, "%s: BF16 is not a packed format here", what);
   if (batch < 0 || rows < 0 || cols < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
   const int64_t elems = batch * rows * cols;
@@ -75,11 +75,14 @@ bsq_status check_packed(const char* what, int32_t fmt, const void* data, const v
   if (fmt == BSQ_NVFP4 && elems > 0 && !ts) return fail(BSQ_ERR_INVALID_ARG, "%s: null tensor_scale", what);
   if (fmt == BSQ_FP8_E4M3_B128 && elems > 0 && !aligned16(scale))
     return fail(BSQ_ERR_INVALID_ARG, "%s: scale_inv not 16-byte aligned", what);
+  if (fmt == BSQ_FP8_E4M3_TENSOR && elems > 0 && (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return fail(BSQ_ERR_INVALID_ARG, "%s: scale_inv not 4-byte aligned", what);
   switch (fmt) {
     case BSQ_BF16:
       if (cols % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: BF16 cols %% 8 != 0 (row pitch must be 16 bytes)", what);
       break;
     case BSQ_FP8_E4M3_B128:
+    case BSQ_FP8_E4M3_TENSOR:
       if (cols % 16) return fail(BSQ_ERR_UNSUPPORTED, "%s: FP8 cols %% 16 != 0 (row pitch must be 16 bytes)", what);
       break;
     case BSQ_MXFP4:
@@ -280,7 +283,7 @@ bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N, int32
   // One launch for both products needs one packed format and enough token rows for the
   // tensor-core dgrad (fewer go to the small-M kernel); otherwise the two entry points run
   // one after the other on the stream.
-  if (w_fmt != x_fmt || M <= bsq::kSmallM || N == 0 || K == 0 || M == 0) {
+  if (bsq::kernel_fmt(w_fmt) != bsq::kernel_fmt(x_fmt) || M <= bsq::kSmallM || N == 0 || K == 0 || M == 0) {
     st = bsq_linear_dgrad(grad_out, M, N, w_fmt, w_data, w_scale, w_tensor_scale, K, grad_x, stream);
     if (st != BSQ_OK) return st;
     return bsq_linear_wgrad(grad_out, M, N, x_fmt, x_data, x_scale, x_tensor_scale, K, grad_w, stream);
@@ -294,7 +297,8 @@ bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N, int32
   d.p_batch = 1; d.p_rows = N; d.kc = K; d.g = grad_out; d.S = M; d.N = N; d.offsets = nullptr; d.E = 1;
   d.out = grad_x; d.stream = static_cast<cudaStream_t>(stream); d.err = err; d.num_sms = sms;
   bsq::GemmArgs w = d;
-  w.op = bsq::kWgrad; w.p_data = x_data; w.p_scale = x_scale; w.p_tensor_scale = x_tensor_scale; w.p_rows = M;
+  w.op = bsq::kWgrad; w.fmt = x_fmt; w.p_data = x_data; w.p_scale = x_scale; w.p_tensor_scale = x_tensor_scale;
+  w.p_rows = M;
   w.out = grad_w;
   const char* msg = "";
   if (bsq::launch_gemm_backward(d, w, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);

@@ -63,17 +63,18 @@ __global__ void __launch_bounds__(kThreads) dequant_fp4_kernel(const uint32_t* _
   }
 }
 
-// FP8 E4M3 with 128x128 scale blocks: 8 codes (uint2) = 16 output bytes per unit.
+// FP8 E4M3 with square scale blocks of side 2^shift (128 x 128 blocks: shift 7; one scale
+// per batch entry: shift 31): 8 codes (uint2) = 16 output bytes per unit.
 __global__ void __launch_bounds__(kThreads) dequant_fp8_kernel(const uint2* __restrict__ data,
                                                                const float* __restrict__ scale_inv,
                                                                int64_t n_units, int64_t rows, int64_t cols,
-                                                               uint4* __restrict__ out) {
+                                                               int shift, uint4* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
   const int64_t units_per_row = cols >> 3;
-  const int64_t rblocks = (rows + 127) >> 7;
-  const int64_t cblocks = (cols + 127) >> 7;
+  const int64_t rblocks = shift >= 31 ? 1 : (rows + (1 << shift) - 1) >> shift;
+  const int64_t cblocks = shift >= 31 ? 1 : (cols + (1 << shift) - 1) >> shift;
   constexpr int64_t kWarpUnits = 32 * kWordsPerLane;
   for (int64_t base = warp * kWarpUnits; base < n_units; base += nwarps * kWarpUnits) {
     uint2 w[kWordsPerLane];
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) dequant_fp8_kernel(const uint2* __re
         const int64_t col = (idx - grow * units_per_row) << 3;
         const int64_t b = grow / rows;
         const int64_t r = grow - b * rows;
-        sv[j] = __ldg(scale_inv + (b * rblocks + (r >> 7)) * cblocks + (col >> 7));
+        sv[j] = __ldg(scale_inv + (b * rblocks + (r >> shift)) * cblocks + (col >> shift));
       }
     }
 #pragma unroll
@@ -130,9 +131,10 @@ int launch_dequant(const DequantArgs& a, const char** msg) {
           a.rows * a.cols / 8, static_cast<uint4*>(a.out));
       break;
     case BSQ_FP8_E4M3_B128:
+    case BSQ_FP8_E4M3_TENSOR:
       dequant_fp8_kernel<<<grid, block, 0, a.stream>>>(static_cast<const uint2*>(a.data),
                                                        static_cast<const float*>(a.scale), units, a.rows, a.cols,
-                                                       static_cast<uint4*>(a.out));
+                                                       fp8_scale_shift(a.fmt), static_cast<uint4*>(a.out));
       break;
     default:
       *msg = "bsq_dequant: format has no packed codes";

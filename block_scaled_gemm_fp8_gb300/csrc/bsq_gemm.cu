@@ -140,7 +140,8 @@ struct Params {
   int32_t num_m;              // ceil(Kc / 128)
   int32_t num_mg;             // ceil(num_m / 2): m-tile pairs, one per pair tile
   int32_t scale_ld;           // scale row pitch (elements)
-  int32_t scale_rblocks;      // FP8: ceil(p_rows / 128)
+  int32_t scale_rblocks;      // FP8: scale rows per batch entry (ceil(p_rows / 128), or 1 per tensor)
+  int32_t scale_shift;        // FP8: log2 of the scale block's side (7; 31 for one scale per tensor)
   int32_t scale_tma;          // FP4: scale tiles come through TMA (row pitch a multiple of 16 bytes)
   int32_t b_mode;             // grad_out half tile per k-block: 0 = two 64x64 boxes, 1 = one 2-D box, 2 = one 3-D box
   int32_t b_rows;             // mode 1: rows of the box (tokens); mode 2: 64-column atoms in the box
@@ -782,13 +783,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t grow = static_cast<int64_t>(pbatch) * gp.p_rows + prow0 + rr;
             if (FMT == BSQ_FP8_E4M3_B128)
               sf[ps] = __ldg(reinterpret_cast<const float*>(gp.scale) +
-                             (static_cast<int64_t>(pbatch) * gp.scale_rblocks + ((prow0 + rr) >> 7)) * p.scale_ld +
-                             (col0 >> 7));
+                             (static_cast<int64_t>(pbatch) * gp.scale_rblocks + ((prow0 + rr) >> gp.scale_shift)) *
+                                 gp.scale_ld +
+                             (col0 >> gp.scale_shift));
             else if (FMT == BSQ_MXFP4 && !gp.scale_tma)
-              sraw[ps] = __ldg(gp.scale + grow * p.scale_ld + (col0 >> 5));
+              sraw[ps] = __ldg(gp.scale + grow * gp.scale_ld + (col0 >> 5));
             else if (FMT == BSQ_NVFP4 && !gp.scale_tma)
-              sraw[ps] = static_cast<uint32_t>(__ldg(gp.scale + grow * p.scale_ld + (col0 >> 4))) |
-                         (static_cast<uint32_t>(__ldg(gp.scale + grow * p.scale_ld + (col0 >> 4) + 1)) << 8);
+              sraw[ps] = static_cast<uint32_t>(__ldg(gp.scale + grow * gp.scale_ld + (col0 >> 4))) |
+                         (static_cast<uint32_t>(__ldg(gp.scale + grow * gp.scale_ld + (col0 >> 4) + 1)) << 8);
           }
         }
         // Both teams wait on every phase of the packed slot (in unit order) and both count
@@ -1048,10 +1050,13 @@ int prepare_op(const GemmArgs& a, OpArgs& o, int64_t* bound, const char** msg) {
   p.Kc = static_cast<int32_t>(a.kc);
   p.num_m = static_cast<int32_t>((a.kc + kTileM - 1) / kTileM);
   p.num_mg = (p.num_m + kPair - 1) / kPair;
+  const bool per_tensor = a.fmt == BSQ_FP8_E4M3_TENSOR;
   p.scale_ld = FMT == BSQ_MXFP4 ? static_cast<int32_t>(a.kc / 32)
                : FMT == BSQ_NVFP4 ? static_cast<int32_t>(a.kc / 16)
+               : per_tensor       ? 1
                                   : static_cast<int32_t>((a.kc + 127) / 128);
-  p.scale_rblocks = static_cast<int32_t>((a.p_rows + 127) / 128);
+  p.scale_rblocks = per_tensor ? 1 : static_cast<int32_t>((a.p_rows + 127) / 128);
+  p.scale_shift = fp8_scale_shift(a.fmt);
   p.timeout_ns = wait_limit_ns();
   const int64_t nn = (a.N + kTileN - 1) / kTileN;
   *bound = dgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
@@ -1130,8 +1135,9 @@ int launch_typed(const GemmArgs* ops, const char** msg) {
 }  // namespace
 
 int launch_gemm(const GemmArgs& a, const char** msg) {
+  const int kf = kernel_fmt(a.fmt);
 #define BSQ_CASE(F_, O_) \
-  if (a.fmt == F_ && a.op == O_) return launch_typed<F_, O_>(&a, msg);
+  if (kf == F_ && a.op == O_) return launch_typed<F_, O_>(&a, msg);
   BSQ_CASE(BSQ_BF16, kDgrad)
   BSQ_CASE(BSQ_BF16, kWgrad)
   BSQ_CASE(BSQ_FP8_E4M3_B128, kDgrad)
@@ -1146,14 +1152,14 @@ int launch_gemm(const GemmArgs& a, const char** msg) {
 }
 
 int launch_gemm_backward(const GemmArgs& dgrad, const GemmArgs& wgrad, const char** msg) {
-  if (dgrad.op != kDgrad || wgrad.op != kWgrad || dgrad.fmt != wgrad.fmt || dgrad.E != wgrad.E ||
+  if (dgrad.op != kDgrad || wgrad.op != kWgrad || kernel_fmt(dgrad.fmt) != kernel_fmt(wgrad.fmt) || dgrad.E != wgrad.E ||
       dgrad.S != wgrad.S || dgrad.N != wgrad.N || dgrad.kc != wgrad.kc || dgrad.g != wgrad.g ||
       dgrad.offsets != wgrad.offsets) {
     *msg = "a fused backward needs one grad_out, one packed format, one K and one set of offsets";
     return -1;
   }
   const GemmArgs ops[2] = {dgrad, wgrad};
-  switch (dgrad.fmt) {
+  switch (kernel_fmt(dgrad.fmt)) {
     case BSQ_BF16: return launch_typed<BSQ_BF16, kBoth>(ops, msg);
     case BSQ_FP8_E4M3_B128: return launch_typed<BSQ_FP8_E4M3_B128, kBoth>(ops, msg);
     case BSQ_MXFP4: return launch_typed<BSQ_MXFP4, kBoth>(ops, msg);

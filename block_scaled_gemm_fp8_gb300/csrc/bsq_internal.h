@@ -20,6 +20,13 @@ constexpr int kTileK = 64;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxDevices = 64;   // device ordinals the per-device host state covers
 
+// The kernels of a format: an FP8 weight with one scale per tensor runs the FP8 kernels,
+// whose scale block is then the whole tensor (fp8_scale_shift).
+inline int kernel_fmt(int fmt) { return fmt == 4 /* BSQ_FP8_E4M3_TENSOR */ ? 1 /* BSQ_FP8_E4M3_B128 */ : fmt; }
+// log2 of the FP8 scale block's side: 7 for 128 x 128 blocks, 31 (every row and column
+// index maps to block 0) for one scale per tensor.
+inline int fp8_scale_shift(int fmt) { return fmt == 4 ? 31 : 7; }
+
 struct GemmArgs {
   int op;            // kDgrad / kWgrad
   int fmt;           // bsq_format of the packed (dequantized) operand

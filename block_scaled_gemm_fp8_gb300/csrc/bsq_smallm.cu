@@ -356,7 +356,8 @@ struct ClusterParams {
   __nv_bfloat16* out;
   int32_t M, N, K;
   int32_t rows_per_split;   // multiple of kChunk
-  int32_t scale_ld;         // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128)
+  int32_t scale_ld;         // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128) (1 with one scale per tensor)
+  int32_t scale_shift;      // FP8: log2 of the scale block's side (7; 31 for one scale per tensor)
   int32_t scale_tma;        // FP4 scale windows through TMA
   uint64_t timeout_ns;
   int32_t* err;
@@ -466,8 +467,9 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
     if (FMT == BSQ_FP8_E4M3_B128) {
       float sf = 0.f;
       if (col_ok && grow0 < n1)
-        sf = __ldg(reinterpret_cast<const float*>(p.scale) + static_cast<int64_t>(grow0 >> 7) * p.scale_ld + (col >> 7));
-      const ScaleBf16 sc = make_scale_fp8(sf);   // one 128-row block holds the whole k-step
+        sf = __ldg(reinterpret_cast<const float*>(p.scale) + static_cast<int64_t>(grow0 >> p.scale_shift) * p.scale_ld +
+                   (col >> p.scale_shift));
+      const ScaleBf16 sc = make_scale_fp8(sf);   // one scale block holds the whole k-step
       uint4 w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(ws_w + rows[i] * F::kRowBytes + 16 * g);
@@ -746,6 +748,7 @@ int launch_smallm(const SmallMArgs& a, const char** msg) {
 }
 
 int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
+  const int fmt = kernel_fmt(a.fmt);
   ClusterParams p;
   p.scale = static_cast<const uint8_t*>(a.w_scale);
   p.tensor_scale = a.w_tensor_scale;
@@ -755,9 +758,11 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   p.K = static_cast<int32_t>(a.K);
   p.err = a.err;
   p.timeout_ns = wait_limit_ns();
-  p.scale_ld = a.fmt == BSQ_MXFP4 ? static_cast<int32_t>(a.K / 32)
-               : a.fmt == BSQ_NVFP4 ? static_cast<int32_t>(a.K / 16)
-                                    : static_cast<int32_t>((a.K + 127) / 128);
+  p.scale_ld = fmt == BSQ_MXFP4 ? static_cast<int32_t>(a.K / 32)
+               : fmt == BSQ_NVFP4 ? static_cast<int32_t>(a.K / 16)
+               : a.fmt == BSQ_FP8_E4M3_TENSOR ? 1
+                                  : static_cast<int32_t>((a.K + 127) / 128);
+  p.scale_shift = fp8_scale_shift(a.fmt);
   const int slabs = static_cast<int>((a.K + kSlab - 1) / kSlab);
   // Row splits = the cluster size: about two CTAs per SM in one wave, at most 8, and no
   // more splits than 64-row chunks.
@@ -770,11 +775,11 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   rps = (rps + kChunk - 1) / kChunk * kChunk;
   p.rows_per_split = static_cast<int32_t>(rps);
   CUtensorMap tm_w, tm_s, tm_g;
-  const uint64_t wrow = a.fmt == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
+  const uint64_t wrow = fmt == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
   {
     const uint64_t dims[2] = {wrow, static_cast<uint64_t>(a.N)};
     const uint64_t strides[1] = {wrow};
-    const uint32_t box[2] = {static_cast<uint32_t>(a.fmt == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2),
+    const uint32_t box[2] = {static_cast<uint32_t>(fmt == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2),
                              static_cast<uint32_t>(kChunk)};
     if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
       *msg = "tensor map encoding failed for W";
@@ -792,8 +797,8 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   }
   tm_s = tm_w;
   p.scale_tma = 0;
-  if (a.fmt == BSQ_MXFP4 || a.fmt == BSQ_NVFP4) {
-    const uint64_t srow = a.fmt == BSQ_MXFP4 ? a.K / 32 : a.K / 16;
+  if (fmt == BSQ_MXFP4 || fmt == BSQ_NVFP4) {
+    const uint64_t srow = fmt == BSQ_MXFP4 ? a.K / 32 : a.K / 16;
     if (srow % 16 == 0 && (reinterpret_cast<uintptr_t>(a.w_scale) & 15u) == 0) {
       const uint64_t dims[2] = {srow, static_cast<uint64_t>(a.N)};
       const uint64_t strides[1] = {srow};
@@ -823,7 +828,7 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   e = cudaFuncSetAttribute(smallm_dgrad_cluster_kernel<F_>, cudaFuncAttributeMaxDynamicSharedMemorySize,           \
                            ClusterFmt<F_>::kSmem);                                                                  \
   if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, smallm_dgrad_cluster_kernel<F_>, tm_w, tm_s, tm_g, p);
-  switch (a.fmt) {
+  switch (fmt) {
     case BSQ_MXFP4: BSQ_LAUNCH_CLUSTER(BSQ_MXFP4) break;
     case BSQ_NVFP4: BSQ_LAUNCH_CLUSTER(BSQ_NVFP4) break;
     case BSQ_FP8_E4M3_B128: BSQ_LAUNCH_CLUSTER(BSQ_FP8_E4M3_B128) break;
@@ -871,9 +876,9 @@ extern "C" bsq_status bsq_linear_dgrad_smallm_noalloc(const void* grad_out, int6
   if (M > bsq::kSmallM)
     return static_cast<bsq_status>(
         bsq::set_error(BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: M must be <= 16"));
-  if (w_fmt == BSQ_BF16)
-    return static_cast<bsq_status>(
-        bsq::set_error(BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: W must be FP8, MXFP4 or NVFP4"));
+  if (w_fmt == BSQ_BF16 || w_fmt == BSQ_FP8_E4M3_TENSOR)
+    return static_cast<bsq_status>(bsq::set_error(
+        BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: W must be FP8 (128x128 blocks), MXFP4 or NVFP4"));
   if (K > kStaticMaxK || bsq::smallm_workspace_bytes(K) > kStaticScratchBytes)
     return static_cast<bsq_status>(bsq::set_error(
         BSQ_ERR_UNSUPPORTED, "bsq_linear_dgrad_smallm_noalloc: K exceeds the static scratch maximum of 16384"));

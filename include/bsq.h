@@ -15,6 +15,7 @@
  *
  * Dequantization rule (bit-exact): out = RNE_bf16( bf16(code value) * RNE_bf16(scale) ).
  *   FP8 E4M3      scale = scale_inv[b][r/128][c/128]                         (float32)
+ *   FP8 E4M3, one scale per tensor:  scale = scale_inv[b]                      (float32)
  *   MXFP4         scale = 2^(e8m0[b][r][c/32] - 127), byte 255 = NaN
  *   NVFP4         scale = RNE_fp32( e4m3[b][r][c/16] * tensor_scale[b] )
  * FP4 packing: byte j of a row holds element 2j in bits 0-3 and 2j+1 in bits 4-7.
@@ -29,12 +30,16 @@
  *       BSQ_BF16           data bf16[batch][rows][cols]; scale, tensor_scale unused
  *       BSQ_FP8_E4M3_B128  data u8  [batch][rows][cols];
  *                          scale f32[batch][ceil(rows/128)][ceil(cols/128)]
+ *       BSQ_FP8_E4M3_TENSOR data u8 [batch][rows][cols]; scale f32[batch] (one scale_inv per
+ *                          tensor -- per expert for a grouped weight -- broadcast over it:
+ *                          transformers PR #50031 `_dequantize_fp8_weight`, block_size None)
  *       BSQ_MXFP4          data u8  [batch][rows][cols/2]; scale u8 [batch][rows][cols/32]
  *       BSQ_NVFP4          data u8  [batch][rows][cols/2]; scale u8 (E4M3) [batch][rows][cols/16];
  *                          tensor_scale f32[batch]
  *   - Alignment: data/scale base pointers 16-byte aligned; the row pitch of every
  *     TMA-read tensor a multiple of 16 bytes, i.e. N % 8 == 0 for grad_out, and
- *     K % 16 (FP8), K % 32 (MXFP4, NVFP4), K % 8 (BF16) for the packed operand.
+ *     K % 16 (both FP8 formats), K % 32 (MXFP4, NVFP4), K % 8 (BF16) for the packed operand;
+ *     a per-tensor FP8 scale array needs only 4-byte alignment.
  *     M, S and the expert sizes are arbitrary.
  *   - Errors: every call validates its arguments on the host first and returns a
  *     status without launching anything when they are wrong.  Nothing is thrown.
@@ -77,7 +82,8 @@ typedef enum {
   BSQ_BF16 = 0,
   BSQ_FP8_E4M3_B128 = 1,
   BSQ_MXFP4 = 2,
-  BSQ_NVFP4 = 3
+  BSQ_NVFP4 = 3,
+  BSQ_FP8_E4M3_TENSOR = 4
 } bsq_format;
 
 /* Device error word values (bsq_get_device_error). */
@@ -89,7 +95,7 @@ typedef enum {
  * bsq_dequant -- decode a packed operand to BF16 (the standalone dequantization the
  * transformers PR #50031 `_dequantize_fp8_weight` performs; MSLK PR #393's FP4
  * dequantization helpers).  out: bf16[batch][rows][cols].  fmt must not be BSQ_BF16.
- * Requirements: cols % 16 == 0 (FP8), cols % 32 == 0 (MXFP4), cols % 16 == 0 (NVFP4).
+ * Requirements: cols % 16 == 0 (both FP8 formats), cols % 32 == 0 (MXFP4), cols % 16 == 0 (NVFP4).
  */
 bsq_status bsq_dequant(int32_t fmt, const void* data, const void* scale, const float* tensor_scale,
                        int64_t batch, int64_t rows, int64_t cols, void* out, void* stream);
@@ -175,7 +181,7 @@ bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N,
  * dgrad kernel that adds its row splits through global memory.  Its FP32 split-K scratch
  * is a file-scope device array of the library; every device that loads the library holds
  * that array (about 1 MiB) until the process exits.
- * Limits: 1 <= M <= 16, w_fmt FP8 / MXFP4 / NVFP4, K <= 16384; anything else returns
+ * Limits: 1 <= M <= 16, w_fmt FP8 (128x128 blocks) / MXFP4 / NVFP4, K <= 16384; anything else returns
  * BSQ_ERR_UNSUPPORTED (or the usual argument errors) without launching.
  * Allocation: calls no cudaMalloc / cudaFree or any allocating routine.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with that device

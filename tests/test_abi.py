@@ -81,3 +81,13 @@ def test_linear_backward_validation(L):
     assert bw(3, gw=None) == bsq.BSQ_ERR_INVALID_ARG
     assert bw(3, xf=9) == bsq.BSQ_ERR_INVALID_ARG
     assert "bsq_linear" in bsq.last_error()
+
+
+def test_fp8_per_tensor_format_validation(L):
+    assert _dgrad(L, fmt=4, K=40) == bsq.BSQ_ERR_UNSUPPORTED            # FP8 row pitch: K % 16
+    assert _dgrad(L, fmt=4, s=FAKE + 2) == bsq.BSQ_ERR_INVALID_ARG       # scale_inv must be 4-byte aligned
+    assert _dgrad(L, fmt=5) == bsq.BSQ_ERR_INVALID_ARG                   # no such format
+    assert L.bsq_dequant(4, FAKE, FAKE + 4, None, 0, 4, 32, FAKE, None) == bsq.BSQ_OK
+    # the allocation-free small-M entry point serves 128 x 128 FP8 blocks only
+    assert L.bsq_linear_dgrad_smallm_noalloc(FAKE, 4, 64, 4, FAKE, FAKE, None, 256, FAKE, None) == \
+        bsq.BSQ_ERR_UNSUPPORTED

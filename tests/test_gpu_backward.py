@@ -18,7 +18,7 @@ from tests._util import assert_gemm, bf16_vals, oracle_deq
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [synth.FMT_BF16, synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4]
+FMTS = [synth.FMT_BF16, synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4, synth.FMT_FP8_TENSOR]
 X_, W_ = bsq.BSQ_NEEDS_GRAD_X, bsq.BSQ_NEEDS_GRAD_W
 
 
@@ -63,7 +63,7 @@ def test_linear_backward_mixed_formats_and_small_m():
     """Formats that differ (the FP8 tiny workload: W E4M3, X BF16) and M <= 16 take the two
     single-product kernels one after the other."""
     for fw, fx, M in [(synth.FMT_FP8, synth.FMT_BF16, 64), (synth.FMT_MXFP4, synth.FMT_MXFP4, 16),
-                      (synth.FMT_NVFP4, synth.FMT_FP8, 5)]:
+                      (synth.FMT_NVFP4, synth.FMT_FP8, 5), (synth.FMT_FP8_TENSOR, synth.FMT_MXFP4, 40)]:
         N, K = 256, 512
         W = synth.make_packed(fw, 1, N, K, 0.5, seed=90, device="cpu")
         X = synth.make_packed(fx, 1, M, K, 1.0, seed=91, device="cpu")
@@ -82,4 +82,21 @@ def test_linear_backward_degenerate_sizes():
     G = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
     gx, gw = _run(G, W, X, X_ | W_, 0, 128, K)
     assert (gw.float() == 0).all().item(), "M = 0: grad_w must be zeros"
+    assert bsq.get_device_error() == (bsq.BSQ_OK, 0)
+
+
+def test_linear_backward_fp8_block_and_tensor_scales_share_a_launch():
+    """W with 128 x 128 scale blocks and X with one scale per tensor run the same FP8
+    kernels, so both products share one launch; each keeps its own scale layout."""
+    M, N, K = 300, 264, 384
+    W = synth.make_packed(synth.FMT_FP8, 1, N, K, 0.5, seed=95, device="cpu")
+    X = synth.make_packed(synth.FMT_FP8_TENSOR, 1, M, K, 1.0, seed=96, device="cpu")
+    G = synth.randn((M, N), 1.0, 97, "cpu", torch.bfloat16)
+    Gd, Wd, Xd = G.cuda(), W.to("cuda"), X.to("cuda")
+    gx, gw = _run(Gd, Wd, Xd, X_ | W_, M, N, K)
+    g, w, x = bf16_vals(G), oracle_deq(W)[0], oracle_deq(X)[0]
+    assert_gemm(bf16_vals(gx), Gm.dgrad(g, w), g, w, N, "dgrad (block scales)")
+    assert_gemm(bf16_vals(gw), Gm.wgrad(g, x), g, x, M, "wgrad (per-tensor scale)")
+    assert torch.equal(_bits(gx), _bits(bsq.linear_dgrad(Gd, Wd)))
+    assert torch.equal(_bits(gw), _bits(bsq.linear_wgrad(Gd, Xd)))
     assert bsq.get_device_error() == (bsq.BSQ_OK, 0)

@@ -31,7 +31,7 @@ from tests._util import oracle_deq
 
 pytestmark = pytest.mark.gpu
 
-PACKED = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4]
+PACKED = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4, synth.FMT_FP8_TENSOR]
 KINDS = ["finite", "nan"]
 FP32_TINY = 2.0 ** -126
 

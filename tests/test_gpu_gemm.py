@@ -19,7 +19,7 @@ from tests._util import assert_gemm, bf16_vals, oracle_deq
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [synth.FMT_BF16, synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4]
+FMTS = [synth.FMT_BF16, synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4, synth.FMT_FP8_TENSOR]
 GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_facts.json")))
 
 

@@ -15,7 +15,7 @@ from tests._util import assert_gemm, bf16_vals, oracle_deq
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4]
+FMTS = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4, synth.FMT_FP8_TENSOR]
 
 
 @pytest.mark.parametrize("fmt", FMTS)
