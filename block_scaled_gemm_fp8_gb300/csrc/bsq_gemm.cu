@@ -146,6 +146,7 @@ struct Params {
   int32_t b_mode;             // grad_out half tile per k-block: 0 = two 64x64 boxes, 1 = one 2-D box, 2 = one 3-D box
   int32_t b_rows;             // mode 1: rows of the box (tokens); mode 2: 64-column atoms in the box
   uint64_t timeout_ns;
+  int32_t drop_announce;      // test hook: the even CTA's relay never announces a unit
 };
 
 struct SharedTail {
@@ -638,8 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(a_full0 + 8 * sl.idx, 4);
-          else st_async_tx_rank(smem_u32(&sh.sink), a_full0 + 8 * sl.idx, 0);
+          if (rank == 0) {
+            if (!p.drop_announce) mbar_arrive_expect_tx(a_full0 + 8 * sl.idx, 4);
+          } else {
+            st_async_tx_rank(smem_u32(&sh.sink), a_full0 + 8 * sl.idx, 0);
+          }
         }
         if (!ok) break;
       }
@@ -1058,6 +1062,11 @@ int prepare_op(const GemmArgs& a, OpArgs& o, int64_t* bound, const char** msg) {
   p.scale_rblocks = per_tensor ? 1 : static_cast<int32_t>((a.p_rows + 127) / 128);
   p.scale_shift = fp8_scale_shift(a.fmt);
   p.timeout_ns = wait_limit_ns();
+  // Test hook (failure detection without a GPU fault): with BSQ_TEST_DROP_ANNOUNCE=1 the
+  // MMA thread's first operand-ready wait can never complete, so it runs out of time and
+  // the kernel takes its orderly abort.
+  const char* drop = std::getenv("BSQ_TEST_DROP_ANNOUNCE");
+  p.drop_announce = drop && drop[0] == '1' ? 1 : 0;
   const int64_t nn = (a.N + kTileN - 1) / kTileN;
   *bound = dgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
   return 0;

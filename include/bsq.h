@@ -60,6 +60,11 @@
  *       BSQ_GEMM_SHORT_TILES  wgrad of a packed format: 1 = the short-tile GEMM kernel (more
  *                             epilogue warps), 0 = the default kernel; unset = the short-tile
  *                             kernel when the groups average fewer than 1024 rows (S < 1024*E).
+ *       BSQ_TEST_DROP_ANNOUNCE test hook for failure detection: 1 = in the GEMM kernels, the
+ *                             even CTA of each pair never announces a unit's operands, so the
+ *                             MMA thread's wait runs out of time (BSQ_WAIT_LIMIT_*), the kernel
+ *                             stops in order and records BSQ_DEVERR_TIMEOUT.  Never set it
+ *                             outside such a test: every GEMM call then fails.
  */
 #ifndef BSQ_H
 #define BSQ_H
