@@ -3,6 +3,7 @@
   grad_X = grad_out @ W_bf16      (dgrad)  -- MSLK PR #393, "Implementation Method";
                                              transformers PR #50031, `FP8LinearFunction.backward`
   grad_W = grad_out^T @ X_bf16    (wgrad)  -- MSLK PR #393, "Implementation Method"
+  Y      = X_bf16 @ W_bf16^T      (forward) -- the product those two are the gradients of
 
 Grouped form (transformers PR #50031, `FP8GroupedMatmulFunction.backward`, and the
 offsets built in `FP8GroupedLinear.forward`): ``offsets`` is an int32 array of E
@@ -35,6 +36,13 @@ def dgrad(grad_out, w):
 def wgrad(grad_out, x):
     """grad_W[N,K] = grad_out[M,N]^T @ X[M,K]."""
     return as_f64(grad_out).T @ as_f64(x)
+
+
+def forward(x, w):
+    """Y[M,N] = X[M,K] @ W[N,K]^T -- the forward of the linear layer whose gradients dgrad and
+    wgrad are (MSLK PR #393, Summary: the `mslk::f4f4bf16` ops multiply packed X and W; the
+    backward the PR adds differentiates that product)."""
+    return as_f64(x) @ as_f64(w).T
 
 
 def expert_rows(offsets, e):

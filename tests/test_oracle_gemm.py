@@ -41,6 +41,32 @@ def test_dgrad_wgrad_brute_force(n):
     assert all(got_w[i][j] == exp_w[i][j] for i in range(n + 1) for j in range(n + 2))
 
 
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_forward_brute_force(n):
+    """Y = X @ W^T against exact rational arithmetic (the contraction is over K, the axis X
+    and W both store contiguously)."""
+    rng = np.random.default_rng(100 + n)
+    x = rng.integers(-40, 40, size=(n, n + 3)) / 64.0
+    w = rng.integers(-40, 40, size=(n + 1, n + 3)) / 64.0
+    exp = _frac_matmul(x.tolist(), w.T.tolist())
+    got = Gm.forward(x, w)
+    assert got.shape == (n, n + 1)
+    assert all(got[i][j] == exp[i][j] for i in range(n) for j in range(n + 1))
+
+
+def test_forward_closed_forms():
+    """One-hot rows of X pick columns of W: Y[i, j] = W[j, k_i]; and the forward is the
+    transpose of a dgrad against the other operand: (X W^T)^T = W X^T."""
+    rng = np.random.default_rng(7)
+    w = rng.standard_normal((6, 9))
+    ks = [0, 4, 8]
+    x = np.zeros((3, 9))
+    x[range(3), ks] = 1.0
+    np.testing.assert_array_equal(Gm.forward(x, w), w[:, ks].T)
+    xr = rng.standard_normal((4, 9))
+    np.testing.assert_allclose(Gm.forward(xr, w).T, Gm.dgrad(w, xr.T), rtol=0, atol=1e-12)
+
+
 def test_bf16_bit_inputs_are_decoded():
     bits = np.array([[0x3F80, 0xC000]], dtype=np.uint16)   # 1.0, -2.0
     w = np.array([[3.0], [0.5]])

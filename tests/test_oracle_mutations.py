@@ -83,3 +83,8 @@ def test_per_tensor_scale_of_the_wrong_expert_is_caught(monkeypatch):
         return real(fmt, scale, tensor_scale, batch, rows, cols)
     monkeypatch.setattr(D, "scale_values", first_expert_only)
     assert _fails(TD.test_fp8_per_tensor_scale_matches_page_recipe, "random")
+
+
+def test_untransposed_forward_is_caught(monkeypatch):
+    monkeypatch.setattr(Gm, "forward", lambda x, w: Gm.as_f64(w) @ Gm.as_f64(x).T)
+    assert _fails(TG.test_forward_brute_force, 3)
