@@ -50,7 +50,8 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the headline workload (not the other four, nor the standalone dequant)")
     ap.add_argument("--profile", default=None,
-                    choices=["backward", "dgrad", "wgrad", "grouped_dgrad", "grouped_wgrad", "small_m", "dequant"],
+                    choices=["backward", "dgrad", "wgrad", "grouped_dgrad", "grouped_wgrad", "small_m", "dequant",
+                             "forward"],
                     help="run only this op of the workload, --warmup + --steps times back to back, and print "
                          "its mean time (a fixed launch sequence for ncu; not a benchmark line)")
     ap.add_argument("--experts", type=int, default=None,
@@ -75,6 +76,9 @@ def profile_run(args, bsq, synth, dev):
         f = lambda: bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=outs["grouped_dgrad"])
     elif op == "grouped_wgrad":
         f = lambda: bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=outs["grouped_wgrad"])
+    elif op == "forward":
+        yo = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
+        f = lambda: bsq.linear_forward(c["X"], c["W"], out=yo)
     elif op == "small_m":
         if "G_small" not in c:
             c["G_small"] = synth.randn((16, c["N"]), 1e-2, 7, dev, torch.bfloat16)
@@ -481,6 +485,8 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     r["tflops"] = fl / (ms * 1e-3) / 1e12
     r["frac_burst"] = r["tflops"] / pk["bf16_tflops"]
     r["frac_sustained"] = r["tflops"] / pk["bf16_tflops_sustained"]
+    if not c["grouped"] and c["X"].fmt != 0:
+        r["forward"] = measure_forward(c, bsq, steps, warmup, flush, pk)
     if n in SMALL_M_WORKLOADS:
         # M = 16 token rows against this workload's weight as well (the split-K kernel)
         if "G_small" not in c:
@@ -494,6 +500,32 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     del c, outs
     torch.cuda.empty_cache()
     return r, deq
+
+
+def measure_forward(c, bsq, steps, warmup, flush, pk):
+    """bsq_linear_forward (Y = X W^T, both packed) on the workload's X and W."""
+    y = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=c["G"].device)
+    for _ in range(warmup):
+        bsq.linear_forward(c["X"], c["W"], out=y)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bsq.linear_forward(c["X"], c["W"], out=y)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    M, N, K = c["M"], c["N"], c["K"]
+    fl = 2.0 * M * N * K
+    nb = packed_bytes(c["X"]) + packed_bytes(c["W"]) + 2.0 * M * N
+    r = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "roofline": op_roofline(fl, nb, ms, pk)}
+    r["roofline"]["traffic"] = profiled_traffic(c["name"], "forward")
+    return r
 
 
 # The standalone dequant is timed on the packed weight of these workloads (one per format);
@@ -702,6 +734,8 @@ def main():
             "per_op_tflops": {o[0]: o[1] / (statistics.median(per_op[o[0]]) * 1e-3) / 1e12 for o in ops},
             "roofline": roof, "gpu_launches": launches, "clocks": clocks}
 
+    if not c["grouped"] and c["X"].fmt != 0:
+        line["forward"] = measure_forward(c, bsq, args.steps, args.warmup, flush, pk)
     if args.config == 2:
         ms, nbytes = time_small_m(c, bsq, args.steps, args.warmup, flush)
         line["small_m_dgrad"] = {"M": int(c["G_small"].shape[0]), "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,

@@ -33,6 +33,8 @@ SIGNATURES = {
                           _c_void_p, _c_void_p],
     "bsq_linear_backward": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p,
                             _c_void_p, _c_void_p, _i64, ctypes.c_uint32, _c_void_p, _c_void_p, _c_void_p],
+    "bsq_linear_forward": [_i32, _c_void_p, _c_void_p, _c_void_p, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64,
+                           _i64, _c_void_p, _c_void_p],
     "bsq_linear_dgrad_smallm_noalloc": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64,
                                         _c_void_p, _c_void_p],
     "bsq_status_string": [_i32],
@@ -165,6 +167,16 @@ def linear_backward(grad_out, w, x, needs=BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD_W, g
         _ptr(grad_x) if needs & BSQ_NEEDS_GRAD_X else None, _ptr(grad_w) if needs & BSQ_NEEDS_GRAD_W else None,
         _stream(stream)))
     return (grad_x if needs & BSQ_NEEDS_GRAD_X else None), (grad_w if needs & BSQ_NEEDS_GRAD_W else None)
+
+
+def linear_forward(x, w, out=None, stream=None):
+    """y[M,N] = deq(X)[M,K] @ deq(W)[N,K]^T with both operands packed."""
+    if out is None:
+        out = torch.empty((x.rows, w.rows), dtype=torch.bfloat16, device=x.data.device)
+    _check(lib().bsq_linear_forward(x.fmt, _ptr(x.data), _ptr(x.scale), _ptr(x.tensor_scale), x.rows, w.fmt,
+                                    _ptr(w.data), _ptr(w.scale), _ptr(w.tensor_scale), w.rows, x.cols, _ptr(out),
+                                    _stream(stream)))
+    return out
 
 
 def grouped_dgrad(grad_out, w, offsets, out=None, stream=None):

@@ -305,6 +305,34 @@ bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N, int32
   return BSQ_OK;
 }
 
+bsq_status bsq_linear_forward(int32_t x_fmt, const void* x_data, const void* x_scale, const float* x_tensor_scale,
+                              int64_t M, int32_t w_fmt, const void* w_data, const void* w_scale,
+                              const float* w_tensor_scale, int64_t N, int64_t K, void* y, void* stream) {
+  const char* what = "bsq_linear_forward";
+  if (M < 0 || N < 0 || K < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
+  bsq_status st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, false);
+  if (st != BSQ_OK) return st;
+  st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, false);
+  if (st != BSQ_OK) return st;
+  if (bsq::kernel_fmt(x_fmt) != bsq::kernel_fmt(w_fmt))
+    return fail(BSQ_ERR_UNSUPPORTED, "%s: X and W must share a packed format (FP8 blocks and per-tensor mix)", what);
+  if (N % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: N %% 8 != 0 (Y row pitch must be 16 bytes)", what);
+  if (x_fmt == BSQ_NVFP4 && K % 32)
+    return fail(BSQ_ERR_UNSUPPORTED, "%s: NVFP4 K %% 32 != 0 (packed row pitch must be 16 bytes)", what);
+  if (M * N > 0 && (!y || !aligned16(y))) return fail(BSQ_ERR_INVALID_ARG, "%s: Y null or not 16-byte aligned", what);
+  if (M == 0 || N == 0) return BSQ_OK;
+  if (K == 0) return zero_output(y, M * N * 2, static_cast<cudaStream_t>(stream), what);
+  int32_t* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  bsq::ForwardArgs a{x_fmt, w_fmt, x_data, x_scale, x_tensor_scale, w_data, w_scale, w_tensor_scale,
+                     M, N, K, y, err, sms, static_cast<cudaStream_t>(stream)};
+  const char* msg = "";
+  if (bsq::launch_forward(a, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
+  return BSQ_OK;
+}
+
 bsq_status bsq_grouped_dgrad(const void* grad_out, int64_t S, int64_t N, int32_t w_fmt, const void* w_data,
                              const void* w_scale, const float* w_tensor_scale, int64_t E, int64_t K,
                              const int32_t* offsets, void* grad_x, void* stream) {

@@ -1,0 +1,547 @@
+// bsq_forward.cu -- the forward product of a block-scaled linear layer, with both operands
+// packed:  Y[M, N] = deq(X)[M, K] @ deq(W)[N, K]^T  (BF16 out, FP32 accumulation).
+//
+// This is the op whose backward the rest of the library computes: MSLK PR #393 adds the
+// backward of its FP4 GEMM ops (`mslk::f4f4bf16` and the grouped forms), whose forward
+// multiplies packed X and W; the backward's gradients grad_X = grad_out @ W and
+// grad_W = grad_out^T @ X are those of Y = X @ W^T.  Both operands are dequantized with the
+// backward's rule (code and scale cast to BF16, product rounded to nearest even) and
+// multiplied on the tensor cores.
+//
+// Both operands have the contraction K as their contiguous axis, so each CTA decodes K-major
+// tiles: its 128 rows of X (the A operand of the 2-SM MMA) and its half of the 256 rows of
+// W (the B operand), 64 k per k-block.  A k-block's decoded elements keep the decode's pair
+// order inside every group of 8 k: both operands use the same order, so the dot products
+// are unchanged.  Output rows are contiguous along the accumulator's columns, so the
+// epilogue writes 16-byte stores.
+//
+// Per CTA, 24 warps (one CTA per SM, clusters of two):
+//   warp 0      TMA producer: packed X and W tiles of each k-block
+//   warp 1      MMA issuer, one thread of the even CTA
+//   warp 2      TMEM allocation; one lane relays "operands ready" to the even CTA
+//   warps 4-7   epilogue
+//   warps 8-23  dequantization, two teams of 8 warps (team t: k-block t of every unit);
+//               each thread decodes 32 k of one row of X and 32 k of one row of W
+// The pair protocol is the backward kernel's: a CTA-local barrier per unit for the
+// dequant warps, then the even relay's arrival and the odd relay's st.async (a release at
+// cluster scope) on the even CTA's barrier, which the MMA thread acquires at cluster scope.
+#include <atomic>
+#include <cstdlib>
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "bsq_decode.cuh"
+#include "bsq_internal.h"
+#include "bsq_pipe.cuh"
+#include "bsq_ptx.cuh"
+#include "../../include/bsq.h"
+
+namespace bsq {
+
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* base, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
+
+namespace {
+
+constexpr int kThreadsF = 768;
+constexpr int kPairF = 2;
+constexpr uint16_t kPairMaskF = 3;
+constexpr int kRowsF = 128;                        // rows of X (and of W's half) per CTA
+constexpr int kKb = 64;                            // k per k-block
+constexpr int kNTile = 256;                        // n per pair tile
+constexpr int kOpBytes = kRowsF * kKb * 2;         // 16 KB: one decoded K-major tile (128 rows x 128 bytes)
+constexpr int kUnit = 2;                           // k-blocks per unit
+constexpr int kOpStages = 2;                       // units of the decoded rings
+constexpr int kOpUnitBytes = kUnit * kOpBytes;     // 32 KB per operand
+constexpr int kTmemColsF = 512;
+constexpr int kDeqWarpsF = 16;
+constexpr int kFirstDeqF = 8;
+
+template <int FMT>
+struct FwdFmt {
+  static constexpr bool kFp4 = FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4;
+  static constexpr int kRowBytes = kFp4 ? kKb / 2 : kKb;          // packed bytes of one row's k-block
+  static constexpr int kTileBytes = kRowsF * kRowBytes;            // one packed tile (X or W half)
+  static constexpr int kStageBytes = 2 * kTileBytes;               // X tile + W tile of a k-block
+  static constexpr int kUnitBytes = kUnit * kStageBytes;
+  static constexpr int kPUnits = kFp4 ? 3 : 2;
+  static constexpr int kRingBytes = 2 * kOpStages * kOpUnitBytes + kPUnits * kUnitBytes;
+};
+
+struct FwdParams {
+  const uint8_t* x_scale;
+  const uint8_t* w_scale;
+  const float* x_ts;           // NVFP4 tensor scales
+  const float* w_ts;
+  __nv_bfloat16* y;
+  int32_t* err;
+  int32_t M, N, K;
+  int32_t num_mp;              // pairs of 128-row blocks of X (pair tiles along M)
+  int32_t num_nt;              // 256-column tiles along N
+  int32_t kblocks;
+  int32_t x_scale_ld, w_scale_ld;      // scale row pitch (elements)
+  int32_t x_shift, w_shift;            // FP8: log2 of the scale block's side (7, or 31 per tensor)
+  uint64_t timeout_ns;
+};
+
+struct FwdShared {
+  uint64_t p_full[4];
+  uint64_t p_empty[4];
+  uint64_t a_local[kOpStages];
+  uint64_t a_full[kOpStages];
+  uint64_t op_empty[kOpStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t sink;
+  uint32_t abort_flag;
+  int32_t pad;
+};
+
+// Scale of 32 k (one thread's share of a k-block row) of a packed operand, in the form
+// decode_row takes: E8M0 byte, two E4M3 bytes, or the FP8 float.
+template <int FMT>
+__device__ __forceinline__ void load_scale(const uint8_t* scale, int ld, int shift, int row, int k0, bool valid,
+                                           uint32_t& sraw, float& sf) {
+  sraw = 0;
+  sf = 0.f;
+  if (!valid) return;
+  if (FMT == BSQ_MXFP4) {
+    sraw = __ldg(scale + static_cast<int64_t>(row) * ld + (k0 >> 5));
+  } else if (FMT == BSQ_NVFP4) {
+    const uint8_t* s = scale + static_cast<int64_t>(row) * ld + (k0 >> 4);
+    sraw = static_cast<uint32_t>(__ldg(s)) | (static_cast<uint32_t>(__ldg(s + 1)) << 8);
+  } else {
+    sf = __ldg(reinterpret_cast<const float*>(scale) + static_cast<int64_t>(row >> shift) * ld + (k0 >> shift));
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ void decode32(const uint4& wa, const uint4& wb, uint32_t sraw, float sf, float ts, bool valid,
+                                         uint32_t (&v)[4][4]) {
+  if (!valid) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[j][i] = 0u;
+    return;
+  }
+  if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) {
+    spread_e2m1x8(wa.x, v[0]);
+    spread_e2m1x8(wa.y, v[1]);
+    spread_e2m1x8(wa.z, v[2]);
+    spread_e2m1x8(wa.w, v[3]);
+    ScaleBf16 s0, s1;
+    if (FMT == BSQ_MXFP4) {
+      s0 = make_scale_e8m0(sraw);
+      s1 = s0;
+    } else {
+      s0 = make_scale_nvfp4(sraw & 0xFFu, ts);
+      s1 = make_scale_nvfp4(sraw >> 8, ts);
+    }
+    scale_pairs4(v[0], s0, kPow2_126x2);
+    scale_pairs4(v[1], s0, kPow2_126x2);
+    scale_pairs4(v[2], s1, kPow2_126x2);
+    scale_pairs4(v[3], s1, kPow2_126x2);
+  } else {
+    decode_e4m3x32(wa, wb, make_scale_fp8(sf), v);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreadsF, 1)
+    bsq_forward_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                       const FwdParams p) {
+  using F = FwdFmt<FMT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring_a = smem;                                   // decoded X tiles (A)
+  uint8_t* ring_b = ring_a + kOpStages * kOpUnitBytes;      // decoded W tiles (B, this CTA's half)
+  uint8_t* ring_p = ring_b + kOpStages * kOpUnitBytes;      // packed X and W tiles
+  FwdShared& sh = *reinterpret_cast<FwdShared*>(smem + F::kRingBytes);
+  volatile uint32_t* abort_flag = &sh.abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < F::kPUnits; ++s) {
+      mbar_init(smem_u32(&sh.p_full[s]), 1);
+      mbar_init(smem_u32(&sh.p_empty[s]), kDeqWarpsF);
+    }
+    for (int s = 0; s < kOpStages; ++s) {
+      mbar_init(smem_u32(&sh.a_local[s]), kDeqWarpsF);
+      mbar_init(smem_u32(&sh.a_full[s]), 1);
+      mbar_init(smem_u32(&sh.op_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh.tmem_full[b]), 1);
+      mbar_init(smem_u32(&sh.tmem_empty[b]), 4);   // even epilogue warps; odd ones: tx bytes
+    }
+    mbar_init(smem_u32(&sh.drain), 1);
+    sh.abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_x);
+    tma_prefetch_map(&tm_w);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(smem_u32(&sh.tmem_base), kTmemColsF);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();
+  const uint32_t tmem_base = sh.tmem_base;
+  const uint64_t limit = p.timeout_ns;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cl_id = blockIdx.x / kPairF, n_cl = gridDim.x / kPairF;
+  const int total_tiles = p.num_mp * p.num_nt;
+  const int units = (p.kblocks + kUnit - 1) / kUnit;
+  uint32_t mma_acc_uses = 0;
+  // tile t: 256 rows of X (128 per CTA) x 256 columns of Y; n-tiles vary slowest so that
+  // consecutive pairs share W tiles in L2
+  auto tile_m0 = [&](int t) { return (t % p.num_mp) * (kPairF * kRowsF) + rank * kRowsF; };
+  auto tile_n0 = [&](int t) { return (t / p.num_mp) * kNTile; };
+  auto mma_n = [&](int t) { return max(32, (min(kNTile, p.N - tile_n0(t)) + 15) & ~15); };
+
+  if (warp == 0) {
+    // ===== TMA producer: packed X and W tiles =====
+    if (lane == 0) {
+      uint32_t uc = 0, pend_mask = 0, pend_par = 0;
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const int m0 = tile_m0(t);
+        const int wrow0 = tile_n0(t) + rank * (mma_n(t) / 2);   // this CTA's half of the tile's W rows
+        bool ok = true;
+        for (int j = 0; j < units; ++j, ++uc) {
+          const Slot sl = ring_slot<F::kPUnits>(uc);
+          if (!wait_phase(smem_u32(&sh.p_empty[sl.idx]), sl.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
+          const uint32_t full = smem_u32(&sh.p_full[sl.idx]);
+          const int nk = min(kUnit, p.kblocks - kUnit * j);
+          mbar_arrive_expect_tx(full, nk * F::kStageBytes);
+          pend_mask |= 1u << sl.idx;
+          pend_par = (pend_par & ~(1u << sl.idx)) | (sl.par << sl.idx);
+          for (int h = 0; h < nk; ++h) {
+            const int kb = kUnit * j + h;
+            uint8_t* dst = ring_p + sl.idx * F::kUnitBytes + h * F::kStageBytes;
+            tma_load_2d(smem_u32(dst), &tm_x, full, kb * F::kRowBytes, m0);
+            tma_load_2d(smem_u32(dst + F::kTileBytes), &tm_w, full, kb * F::kRowBytes, wrow0);
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) drain_pending<F::kPUnits>(sh.p_full, pend_mask, pend_par, kDrainLimitNs);
+    }
+  } else if (warp == 1) {
+    // ===== MMA issuer (even CTA): 4 MMAs of K 16 per k-block, both operands K-major =====
+    if (lane == 0 && rank == 0) {
+      uint32_t iu = 0, pu = 0;
+      uint32_t& acc = mma_acc_uses;
+      const uint64_t adesc0 = sdesc_sw128(smem_u32(ring_a), 16, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(smem_u32(ring_b), 16, 1024);
+      const uint32_t a_full0 = smem_u32(&sh.a_full[0]), op_empty0 = smem_u32(&sh.op_empty[0]);
+      auto ready = [&](uint32_t s, uint32_t q) { return wait_phase<true>(a_full0 + 8 * s, q, abort_flag, p.err, limit); };
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const uint32_t buf = acc & 1u;
+        const uint32_t acc_phase = (acc >> 1) & 1u;
+        if (!wait_phase<true>(smem_u32(&sh.tmem_empty[buf]), acc_phase ^ 1u, abort_flag, p.err, limit)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(kPairF * kRowsF, static_cast<uint32_t>(mma_n(t)), false, false);
+        const uint32_t d_tmem = tmem_base + buf * kNTile;
+        bool ok = ready(iu, pu);
+        for (int j = 0; ok && j < units; ++j) {
+          const int nk = min(kUnit, p.kblocks - kUnit * j);
+          tc_fence_after();
+          const uint64_t ad = adesc0 + iu * (kOpUnitBytes >> 4);
+          const uint64_t bd = bdesc0 + iu * (kOpUnitBytes >> 4);
+#pragma unroll
+          for (int h = 0; h < kUnit; ++h)
+            if (h < nk)
+              umma_bf16_pair_k64_kmajor(d_tmem, ad + h * (kOpBytes >> 4), bd + h * (kOpBytes >> 4), idesc,
+                                        (j | h) != 0 ? 1u : 0u);
+          const uint32_t su = iu;
+          if (++iu == kOpStages) {
+            iu = 0;
+            pu ^= 1u;
+          }
+          if (j + 1 < units) ok = ready(iu, pu);
+          umma_commit_pair(op_empty0 + 8 * su, kPairMaskF);
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&sh.tmem_full[buf]), kPairMaskF);
+        ++acc;
+      }
+    }
+  } else if (warp == 2) {
+    // ===== operand-ready relay =====
+    if (lane == 0) {
+      uint32_t uc = 0;
+      const uint32_t a_full0 = smem_u32(&sh.a_full[0]);
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        bool ok = true;
+        for (int j = 0; j < units; ++j, ++uc) {
+          const Slot sl = ring_slot<kOpStages>(uc);
+          if (!wait_phase(smem_u32(&sh.a_local[sl.idx]), sl.par, abort_flag, p.err, limit)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(a_full0 + 8 * sl.idx, 4);
+          else st_async_tx_rank(smem_u32(&sh.sink), a_full0 + 8 * sl.idx, 0);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ===== epilogue: lane = row of Y, 16 consecutive columns per TMEM load, 16-byte stores =====
+    const int q = warp & 3;
+    uint32_t acc = 0;
+    for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+      const int m = tile_m0(t) + q * 32 + lane;
+      const int n0 = tile_n0(t);
+      const int n_valid = min(kNTile, p.N - n0);
+      const uint32_t buf = acc & 1u;
+      const uint32_t acc_phase = (acc >> 1) & 1u;
+      ++acc;
+      bool ok = wait_phase(smem_u32(&sh.tmem_full[buf]), acc_phase, abort_flag, p.err, limit);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int nchunks = (n_valid + 15) >> 4;
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kNTile;
+      __nv_bfloat16* yrow = p.y + static_cast<int64_t>(m) * p.N + n0;
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(trow, v);
+      for (int c = 0; c < nchunks; ++c) {
+        tmem_wait_ld();
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        if (c + 1 < nchunks) {
+          tmem_ld_32x32b_x16(trow + (c + 1) * 16, v);
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&sh.tmem_empty[buf]), 4);
+            else st_async_tx_rank(smem_u32(&sh.sink), smem_u32(&sh.tmem_empty[buf]), 0);
+          }
+        }
+        if (m < p.M) {
+          const int nlim = min(16, n_valid - c * 16);
+          __nv_bfloat16* o = yrow + c * 16;
+          if (nlim == 16) {
+            uint4* o4 = reinterpret_cast<uint4*>(o);   // N % 8 == 0: 16-byte aligned
+            o4[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            o4[1] = make_uint4(h[4], h[5], h[6], h[7]);
+          } else {
+            unsigned short* os = reinterpret_cast<unsigned short*>(o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nlim) os[j] = static_cast<unsigned short>((j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
+          }
+        }
+      }
+    }
+  } else if (warp >= kFirstDeqF) {
+    // ===== dequantization: thread -> row r of the k-block, k half hk (32 k) =====
+    const int dq = warp - kFirstDeqF;
+    const int team = dq / 8;
+    const int tt = (dq % 8) * 32 + lane;         // 0..255 within the team
+    const int r = tt >> 1, hk = tt & 1;
+    const uint32_t a_ring = smem_u32(ring_a), b_ring = smem_u32(ring_b), p_ring = smem_u32(ring_p);
+    // swizzled 16-byte slots of the thread's four 8-k groups in a K-major tile row r
+    uint32_t st_off[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) st_off[j] = r * 128 + (((4 * hk + j) ^ (r & 7)) << 4);
+    const uint32_t p_off = r * F::kRowBytes + hk * (F::kRowBytes / 2);
+    float xts = 0.f, wts = 0.f;
+    if (FMT == BSQ_NVFP4) {
+      xts = __ldg(p.x_ts);
+      wts = __ldg(p.w_ts);
+    }
+    uint32_t uc = 0;
+    bool ok = true;
+    for (int t = cl_id; ok && t < total_tiles && !*abort_flag; t += n_cl) {
+      const int xrow = tile_m0(t) + r;
+      const int wrow = tile_n0(t) + rank * (mma_n(t) / 2) + r;
+      const bool xok = xrow < p.M, wok = wrow < p.N && r < mma_n(t) / 2;
+      for (int j = 0; j < units; ++j) {
+        const int kb = kUnit * j + team;
+        const bool present = kb < p.kblocks;
+        const Slot sa = ring_slot<kOpStages>(uc + j);
+        const Slot sp = ring_slot<F::kPUnits>(uc + j);
+        const int k0 = kb * kKb + 32 * hk;
+        const bool kok = present && k0 < p.K;
+        uint32_t xs, ws;
+        float xf, wf;
+        load_scale<FMT>(p.x_scale, p.x_scale_ld, p.x_shift, xrow, k0, kok && xok, xs, xf);
+        load_scale<FMT>(p.w_scale, p.w_scale_ld, p.w_shift, wrow, k0, kok && wok, ws, wf);
+        ok = wait_phase(smem_u32(&sh.p_full[sp.idx]), sp.par, abort_flag, p.err, limit);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint32_t pst = p_ring + sp.idx * F::kUnitBytes + team * F::kStageBytes;
+        uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, wa = xa, wb = xa;
+        if (kok && xok) {
+          xa = lds128(pst + p_off);
+          if (!F::kFp4) xb = lds128(pst + p_off + 16);
+        }
+        if (kok && wok) {
+          wa = lds128(pst + F::kTileBytes + p_off);
+          if (!F::kFp4) wb = lds128(pst + F::kTileBytes + p_off + 16);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));
+        uint32_t v[4][4];
+        decode32<FMT>(xa, xb, xs, xf, xts, kok && xok, v);
+        ok = wait_phase(smem_u32(&sh.op_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (present) {
+          const uint32_t at = a_ring + sa.idx * kOpUnitBytes + team * kOpBytes;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) sts128(at + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
+          decode32<FMT>(wa, wb, ws, wf, wts, kok && wok, v);
+          const uint32_t bt = b_ring + sa.idx * kOpUnitBytes + team * kOpBytes;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) sts128(bt + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.a_local[sa.idx]));
+      }
+      uc += units;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == 1 && lane == 0 && rank == 0) {
+    umma_commit_pair(smem_u32(&sh.drain), 1);
+    uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(smem_u32(&sh.drain), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+    }
+    if (!*abort_flag) {
+      for (uint32_t b = 0; b < 2; ++b) {
+        const uint32_t uses = (mma_acc_uses + 1u - b) / 2u;
+        if (uses == 0) continue;
+        t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&sh.tmem_empty[b]), (uses - 1u) & 1u) && global_timer_ns() - t0 < kDrainLimitNs) {
+        }
+      }
+    }
+  }
+  if (rank == 0 && *abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < kAbortSettleNs) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();
+  if (warp == 2) tmem_dealloc_pair(tmem_base, kTmemColsF);
+}
+
+template <int FMT>
+int launch_forward_typed(const ForwardArgs& a, const char** msg) {
+  using F = FwdFmt<FMT>;
+  CUtensorMap tm_x, tm_w;
+  const uint64_t row_bytes = FMT == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
+  {
+    const uint64_t dims[2] = {row_bytes, static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {static_cast<uint32_t>(F::kRowBytes), static_cast<uint32_t>(kRowsF)};
+    if (!encode_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.x_data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      *msg = "tensor map encoding failed for X";
+      return -1;
+    }
+  }
+  {
+    const uint64_t dims[2] = {row_bytes, static_cast<uint64_t>(a.N)};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {static_cast<uint32_t>(F::kRowBytes), static_cast<uint32_t>(kRowsF)};
+    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      *msg = "tensor map encoding failed for W";
+      return -1;
+    }
+  }
+  FwdParams p;
+  p.x_scale = static_cast<const uint8_t*>(a.x_scale);
+  p.w_scale = static_cast<const uint8_t*>(a.w_scale);
+  p.x_ts = a.x_tensor_scale;
+  p.w_ts = a.w_tensor_scale;
+  p.y = static_cast<__nv_bfloat16*>(a.y);
+  p.err = a.err;
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.K = static_cast<int32_t>(a.K);
+  p.num_mp = static_cast<int32_t>((a.M + kPairF * kRowsF - 1) / (kPairF * kRowsF));
+  p.num_nt = static_cast<int32_t>((a.N + kNTile - 1) / kNTile);
+  p.kblocks = static_cast<int32_t>((a.K + kKb - 1) / kKb);
+  auto ld = [&](int fmt) {
+    return fmt == BSQ_MXFP4 ? static_cast<int32_t>(a.K / 32)
+           : fmt == BSQ_NVFP4 ? static_cast<int32_t>(a.K / 16)
+           : fmt == BSQ_FP8_E4M3_TENSOR ? 1
+                                : static_cast<int32_t>((a.K + 127) / 128);
+  };
+  p.x_scale_ld = ld(a.x_fmt);
+  p.w_scale_ld = ld(a.w_fmt);
+  p.x_shift = fp8_scale_shift(a.x_fmt);
+  p.w_shift = fp8_scale_shift(a.w_fmt);
+  p.timeout_ns = wait_limit_ns();
+  static_assert(F::kRingBytes + sizeof(FwdShared) + 1024 <= 232448, "rings exceed the shared memory of a CTA");
+  const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(FwdShared) + 1024;
+  auto kern = bsq_forward_kernel<FMT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPairF;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreadsF);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static std::atomic<int> max_clusters_of[kMaxDevices];
+  int dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
+  int max_clusters = e == cudaSuccess ? max_clusters_of[dev].load() : 0;
+  if (e == cudaSuccess && max_clusters == 0) {
+    cfg.gridDim = dim3(kPairF * (a.num_sms / kPairF));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    max_clusters = n > 0 ? n : a.num_sms / kPairF;
+    max_clusters_of[dev].store(max_clusters);
+  }
+  const int64_t tiles = static_cast<int64_t>(p.num_mp) * p.num_nt;
+  int64_t clusters = tiles < max_clusters ? tiles : max_clusters;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kPairF));
+  if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *msg = cudaGetErrorString(e);
+    return static_cast<int>(e);
+  }
+  return 0;
+}
+
+}  // namespace
+
+int launch_forward(const ForwardArgs& a, const char** msg) {
+  switch (kernel_fmt(a.x_fmt)) {
+    case BSQ_FP8_E4M3_B128: return launch_forward_typed<BSQ_FP8_E4M3_B128>(a, msg);
+    case BSQ_MXFP4: return launch_forward_typed<BSQ_MXFP4>(a, msg);
+    case BSQ_NVFP4: return launch_forward_typed<BSQ_NVFP4>(a, msg);
+    default: break;
+  }
+  *msg = "forward: unsupported format";
+  return -1;
+}
+
+}  // namespace bsq

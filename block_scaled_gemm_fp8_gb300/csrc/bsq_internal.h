@@ -87,6 +87,23 @@ int launch_smallm(const SmallMArgs& a, const char** msg);
 // cluster (distributed shared memory): no workspace (a.ws is not used).
 int launch_smallm_cluster(const SmallMArgs& a, const char** msg);
 
+struct ForwardArgs {
+  int x_fmt, w_fmt;        // packed formats of X and W (one kernel format: kernel_fmt equal)
+  const void* x_data;      // packed [M][K]
+  const void* x_scale;
+  const float* x_tensor_scale;
+  const void* w_data;      // packed [N][K]
+  const void* w_scale;
+  const float* w_tensor_scale;
+  int64_t M, N, K;
+  void* y;                 // bf16 [M][N]
+  int32_t* err;
+  int num_sms;
+  cudaStream_t stream;
+};
+// Y = deq(X) @ deq(W)^T (bsq_forward.cu).
+int launch_forward(const ForwardArgs& a, const char** msg);
+
 // Host-side argument checks of bsq_linear_dgrad (bsq_api.cu); BSQ_OK when well formed.
 int check_linear_dgrad_args(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
                             const void* w_scale, const float* w_tensor_scale, int64_t K, const void* grad_x);

@@ -190,6 +190,23 @@ __device__ __forceinline__ void umma_bf16_pair_k64(uint32_t d_tmem, uint64_t a_d
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP)
       : "memory");
 }
+// As umma_bf16_pair_k64 with both operands K-major (128-byte swizzled rows of 64 k): both
+// descriptors advance 32 bytes per 16 k.
+__device__ __forceinline__ void umma_bf16_pair_k64_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 q, %4, %4;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on the barrier at the same offset in every CTA of `mask` when every pair MMA
 // this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {

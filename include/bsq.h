@@ -154,6 +154,21 @@ bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N,
                                int64_t K, uint32_t needs, void* grad_x, void* grad_w, void* stream);
 
 /*
+ * bsq_linear_forward -- y[M][N] = deq(X)[M][K] @ deq(W)[N][K]^T, the forward product of the
+ * layer the entry points above differentiate (MSLK PR #393, Summary: the mslk::f4f4bf16 ops
+ * multiply packed X and W; the backward the PR adds is that of this product).  Both
+ * operands are dequantized with the rule above, multiplied on the tensor cores with FP32
+ * accumulation and rounded once to BF16.
+ * X: packed [1][M][K] in x_fmt, W: packed [1][N][K] in w_fmt; both packed (not BSQ_BF16) and
+ * of one kind: both FP4 of one format, or both FP8 (128x128 blocks or per tensor, mixed).
+ * y: bf16[M][N], fully written; N % 8 == 0.  K == 0 gives zeros.
+ */
+bsq_status bsq_linear_forward(int32_t x_fmt, const void* x_data, const void* x_scale,
+                              const float* x_tensor_scale, int64_t M,
+                              int32_t w_fmt, const void* w_data, const void* w_scale,
+                              const float* w_tensor_scale, int64_t N, int64_t K, void* y, void* stream);
+
+/*
  * bsq_grouped_dgrad -- per expert e, grad_x[r0:r1] = grad_out[r0:r1] @ deq(W[e])
  * (transformers PR #50031 FP8GroupedMatmulFunction.backward).
  * offsets: device int32[E], cumulative END offsets without a leading zero

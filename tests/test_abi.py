@@ -91,3 +91,13 @@ def test_fp8_per_tensor_format_validation(L):
     # the allocation-free small-M entry point serves 128 x 128 FP8 blocks only
     assert L.bsq_linear_dgrad_smallm_noalloc(FAKE, 4, 64, 4, FAKE, FAKE, None, 256, FAKE, None) == \
         bsq.BSQ_ERR_UNSUPPORTED
+
+
+def test_linear_forward_validation(L):
+    def fw(xf=2, wf=2, M=64, N=128, K=256, y=FAKE):
+        return L.bsq_linear_forward(xf, FAKE, FAKE, FAKE, M, wf, FAKE, FAKE, FAKE, N, K, y, None)
+    assert fw(xf=0) == bsq.BSQ_ERR_UNSUPPORTED          # BF16 X is not a packed operand
+    assert fw(xf=2, wf=3) == bsq.BSQ_ERR_UNSUPPORTED    # MXFP4 x NVFP4: no common kernel
+    assert fw(N=12) == bsq.BSQ_ERR_UNSUPPORTED          # Y row pitch
+    assert fw(y=None) == bsq.BSQ_ERR_INVALID_ARG
+    assert fw(M=0) == bsq.BSQ_OK and fw(N=0) == bsq.BSQ_OK
