@@ -56,12 +56,16 @@ def parse_args():
                          "its mean time (a fixed launch sequence for ncu; not a benchmark line)")
     ap.add_argument("--experts", type=int, default=None,
                     help="grouped workloads: scale down to this many experts (same tokens per expert)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="workload 4 with --profile: route this many grad_out rows (a decode-sized batch) "
+                         "over the same 64 expert weights")
     return ap.parse_args()
 
 
 def profile_run(args, bsq, synth, dev):
     """--profile: one op of the workload, back to back (no L2 flush in between)."""
-    c = synth.make_config(args.config, device=dev, seed=0, experts=args.experts)
+    c = synth.make_config(args.config, device=dev, seed=0, experts=args.experts,
+                          rows=args.rows if args.config == 4 else None)
     if c["grouped"]:
         c["offsets_dev"] = torch.from_numpy(c["offsets"]).to(dev)
     outs = alloc_outputs(c, dev)

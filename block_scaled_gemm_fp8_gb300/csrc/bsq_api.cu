@@ -346,11 +346,33 @@ bsq_status bsq_grouped_dgrad(const void* grad_out, int64_t S, int64_t N, int32_t
   if (st != BSQ_OK) return st;
   if (S == 0 || K == 0) return BSQ_OK;
   if (N == 0) return fail(BSQ_ERR_UNSUPPORTED, "%s: N == 0 with S > 0 (rows to zero depend on offsets)", what);
-  bsq::GemmArgs a{};
-  a.op = bsq::kDgrad; a.fmt = w_fmt; a.p_data = w_data; a.p_scale = w_scale; a.p_tensor_scale = w_tensor_scale;
-  a.p_batch = E; a.p_rows = N; a.kc = K; a.g = grad_out; a.S = S; a.N = N; a.offsets = offsets; a.E = E;
-  a.out = grad_x; a.stream = static_cast<cudaStream_t>(stream);
-  return run_gemm(a, what);
+  // A decode-sized call (S within the small-rows bound) is bound by reading the experts'
+  // weights, not by the tensor cores: the small-M kernel computes every row.  Above the
+  // bound the pair-tile GEMM does, less (when a tail bound is set) each expert's ragged
+  // last tile of at most that many rows, which the small-M kernel then takes.  Both read
+  // the same device offsets, so each row has exactly one owner.
+  const bool packed_w = w_fmt != BSQ_BF16;
+  int tail = 0;
+  if (!packed_w || S > bsq::grouped_small_rows()) {
+    tail = packed_w ? bsq::grouped_tail_rows() : 0;
+    bsq::GemmArgs a{};
+    a.op = bsq::kDgrad; a.fmt = w_fmt; a.p_data = w_data; a.p_scale = w_scale; a.p_tensor_scale = w_tensor_scale;
+    a.p_batch = E; a.p_rows = N; a.kc = K; a.g = grad_out; a.S = S; a.N = N; a.offsets = offsets; a.E = E;
+    a.out = grad_x; a.stream = static_cast<cudaStream_t>(stream); a.tail_rows = tail;
+    st = run_gemm(a, what);
+    if (st != BSQ_OK || tail == 0) return st;
+  } else {
+    tail = bsq::kTileN - 1;   // every expert here has fewer than kTileN rows: all of them
+  }
+  int32_t* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  bsq::SmallMArgs s{w_fmt, grad_out, w_data, w_scale, w_tensor_scale, S, N, K, grad_x, nullptr, sms,
+                    static_cast<cudaStream_t>(stream), err, offsets, E, tail};
+  const char* msg = "";
+  if (bsq::launch_smallm_cluster(s, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
+  return BSQ_OK;
 }
 
 bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N, int32_t x_fmt, const void* x_data,

@@ -142,9 +142,13 @@ __device__ __forceinline__ void spread_e4m3x4(uint32_t w, uint32_t& a, uint32_t&
   b = (prmt(w, 0u, 0xB391u) << 4) & 0x87F087F0u;
 }
 
-__device__ __forceinline__ bool e4m3_any_nan(uint32_t w) {
-  return (((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u;
-}
+// Bit 7 of byte j of the result is set exactly when byte j of w is an E4M3 NaN code
+// (S.1111.111): the low seven bits plus one reach 0x80 only from 0x7F, and no carry leaves
+// a byte.  Several words are tested at once by OR-ing their marks (not the words: an OR of
+// codes gathers the bits of different codes and nearly always looks like 0x7F).
+__device__ __forceinline__ uint32_t e4m3_nan_mark(uint32_t w) { return (w & 0x7F7F7F7Fu) + 0x01010101u; }
+__device__ __forceinline__ bool e4m3_marked(uint32_t marks) { return (marks & 0x80808080u) != 0u; }
+__device__ __forceinline__ bool e4m3_any_nan(uint32_t w) { return e4m3_marked(e4m3_nan_mark(w)); }
 
 // Overwrite the NaN codes of word w in its decoded pairs with BF16 NaN.
 __device__ __forceinline__ void e4m3_fix_nan(uint32_t w, uint32_t& p02, uint32_t& p13) {
@@ -169,15 +173,15 @@ __device__ __forceinline__ void decode_e4m3x8(uint32_t w0, uint32_t w1, const Sc
   spread_e4m3x4(w0, out[0], out[1]);
   spread_e4m3x4(w1, out[2], out[3]);
   scale_pairs4(out, s, kPow2_120x2);
-  if (e4m3_any_nan(w0 | w1)) {  // conservative: OR can only add candidates, the fix checks bytes
+  if (e4m3_marked(e4m3_nan_mark(w0) | e4m3_nan_mark(w1))) {
     e4m3_fix_nan(w0, out[0], out[1]);
     e4m3_fix_nan(w1, out[2], out[3]);
   }
 }
 
 // 32 E4M3 codes of one row (lo = codes 0..15, hi = codes 16..31, element j of a word in
-// byte j) -> groups out[g] = decode_e4m3x8 of codes 8g..8g+7, scaled; one NaN test covers
-// all 32 codes (an OR can only add candidates, the fix checks each byte).
+// byte j) -> groups out[g] = decode_e4m3x8 of codes 8g..8g+7, scaled; one exact NaN test
+// covers all 32 codes, and only a row holding a NaN code takes the byte-by-byte fix.
 __device__ __forceinline__ void decode_e4m3x32(const uint4& lo, const uint4& hi, const ScaleBf16& s,
                                                uint32_t (&out)[4][4]) {
   spread_e4m3x4(lo.x, out[0][0], out[0][1]);
@@ -190,7 +194,8 @@ __device__ __forceinline__ void decode_e4m3x32(const uint4& lo, const uint4& hi,
   spread_e4m3x4(hi.w, out[3][2], out[3][3]);
 #pragma unroll
   for (int g = 0; g < 4; ++g) scale_pairs4(out[g], s, kPow2_120x2);
-  if (e4m3_any_nan(lo.x | lo.y | lo.z | lo.w | hi.x | hi.y | hi.z | hi.w)) {
+  if (e4m3_marked(e4m3_nan_mark(lo.x) | e4m3_nan_mark(lo.y) | e4m3_nan_mark(lo.z) | e4m3_nan_mark(lo.w) |
+                  e4m3_nan_mark(hi.x) | e4m3_nan_mark(hi.y) | e4m3_nan_mark(hi.z) | e4m3_nan_mark(hi.w))) {
     e4m3_fix_nan(lo.x, out[0][0], out[0][1]);
     e4m3_fix_nan(lo.y, out[0][2], out[0][3]);
     e4m3_fix_nan(lo.z, out[1][0], out[1][1]);

@@ -148,6 +148,8 @@ struct Params {
   int32_t b_rows;             // mode 1: rows of the box (tokens); mode 2: 64-column atoms in the box
   uint64_t timeout_ns;
   int32_t drop_announce;      // test hook: the even CTA's relay never announces a unit
+  int32_t tail_rows;          // grouped dgrad: an expert's last (rows % kTileN) rows, when at most
+                              // this many, are left to the small-M kernel (0: none)
 };
 
 struct SharedTail {
@@ -173,9 +175,15 @@ struct TileInfo {
 
 // Pair tiles of an expert with cnt rows, and one past the last row of expert e (the
 // cumulative end offset; a null offsets pointer is one group of S rows).
+// Rows of an expert's dgrad that the pair tiles take: all of them, less a ragged last tile
+// of 1..tail_rows rows (the small-M kernel's share; the same rule is applied there).
+__device__ __forceinline__ int dgrad_tile_rows(const Params& p, int cnt) {
+  const int tail = cnt % kTileN;
+  return (tail > 0 && tail <= p.tail_rows) ? cnt - tail : cnt;
+}
 template <int OP>
 __device__ __forceinline__ int expert_tiles(const Params& p, int cnt) {
-  const int ntiles = OP == kDgrad ? (cnt + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
+  const int ntiles = OP == kDgrad ? (dgrad_tile_rows(p, cnt) + kTileN - 1) / kTileN : (p.N + kTileN - 1) / kTileN;
   return ntiles * p.num_mg;
 }
 __device__ __forceinline__ int expert_end(const Params& p, int e) { return p.offsets ? __ldg(p.offsets + e) : p.S; }
@@ -214,7 +222,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, ExpertCursor& c, const Pa
   ti.r1 = c.r1;
   const int cnt = ti.r1 - ti.r0;
   if (OP == kDgrad) {
-    ti.n_valid = min(kTileN, cnt - ti.nt * kTileN);
+    ti.n_valid = min(kTileN, dgrad_tile_rows(p, cnt) - ti.nt * kTileN);
     ti.kblocks = (p.N + kTileK - 1) / kTileK;
   } else {
     ti.n_valid = min(kTileN, p.N - ti.nt * kTileN);
@@ -1018,6 +1026,7 @@ int prepare_op(const GemmArgs& a, OpArgs& o, int64_t* bound, const char** msg) {
   // the kernel takes its orderly abort.
   const char* drop = std::getenv("BSQ_TEST_DROP_ANNOUNCE");
   p.drop_announce = drop && drop[0] == '1' ? 1 : 0;
+  p.tail_rows = dgrad && a.offsets ? a.tail_rows : 0;
   const int64_t nn = (a.N + kTileN - 1) / kTileN;
   *bound = dgrad ? p.num_mg * ((a.S + kTileN - 1) / kTileN + a.E) : p.num_mg * nn * a.E;
   return 0;

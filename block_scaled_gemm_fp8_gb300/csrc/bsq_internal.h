@@ -45,6 +45,8 @@ struct GemmArgs {
   int32_t* err;      // device error word
   int num_sms;
   cudaStream_t stream;
+  int tail_rows;     // grouped dgrad: ragged last tiles of 1..tail_rows rows are left out
+                     // (the small-M kernel's share, same rule); 0 = none
 };
 
 // Returns a cudaError_t-style code (0 = launched) and fills `msg` on failure.
@@ -68,24 +70,36 @@ int launch_dequant(const DequantArgs& a, const char** msg);
 
 struct SmallMArgs {
   int fmt;
-  const void* g;          // bf16 [M][N]
-  const void* w_data;     // packed [N][K]
+  const void* g;          // bf16 [M][N] (grouped: [S][N], M = S)
+  const void* w_data;     // packed [N][K] (grouped: [E][N][K])
   const void* w_scale;
-  const float* w_tensor_scale;
-  int64_t M, N, K;        // M <= 16
+  const float* w_tensor_scale;   // NVFP4: f32[E]
+  int64_t M, N, K;        // linear: M <= 16
   void* out;              // bf16 [M][K]
   void* ws;               // FP32 workspace of smallm_workspace_bytes(K) bytes, zero between calls
   int num_sms;
   cudaStream_t stream;
   int32_t* err;           // device error word
+  const int32_t* offsets = nullptr;   // grouped (cluster kernel only): device cumulative ends [E]
+  int64_t E = 1;
+  int tail_rows = 0;      // grouped: rows of an expert taken (its ragged last GEMM tile, 1..tail_rows rows)
 };
 
 constexpr int kSmallM = 16;  // dgrad with at most this many rows takes the split-K kernel
 size_t smallm_workspace_bytes(int64_t K);
 int launch_smallm(const SmallMArgs& a, const char** msg);
 // The same product with the row splits of a column slab reduced inside a thread-block
-// cluster (distributed shared memory): no workspace (a.ws is not used).
+// cluster (distributed shared memory): no workspace (a.ws is not used).  With offsets it
+// is the grouped dgrad of the rows that the pair-tile GEMM leaves out (GemmArgs::tail_rows).
 int launch_smallm_cluster(const SmallMArgs& a, const char** msg);
+// Grouped dgrad with at most this many grad_out rows in all goes wholly to the small-M
+// kernel (BSQ_GROUPED_SMALL_ROWS overrides, 0..255; 0 never).
+constexpr int kGroupedSmallRows = 64;
+int grouped_small_rows();
+// Above that, an expert's ragged last pair tile of at most this many rows goes to the
+// small-M kernel and the rest to the GEMM (BSQ_GROUPED_TAIL_ROWS, 0..255; default 0: the
+// GEMM takes every row).
+int grouped_tail_rows();
 
 struct ForwardArgs {
   int x_fmt, w_fmt;        // packed formats of X and W (one kernel format: kernel_fmt equal)

@@ -103,6 +103,11 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 // 32-bit store to the same offset in CTA `rank`.
 __device__ __forceinline__ void st_rank_u32(uint32_t addr, uint32_t rank, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_rank(addr, rank)), "r"(v) : "memory");
@@ -280,6 +285,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
   return v;
 }
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {

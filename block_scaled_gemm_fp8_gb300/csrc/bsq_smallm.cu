@@ -18,7 +18,9 @@
 //     (the allocation-free entry point) adds into an FP32 scratch with 16-byte reduction
 //     atomics, and the last CTA of a slab converts it to BF16, writes grad_X and zeroes the
 //     scratch again.
+#include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -342,23 +344,36 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
 }
 
 // ---------------------------------------------------------------- cluster-reduced variant
-// The same product without any global workspace: the CTAs that split a column slab's rows
-// form one thread-block cluster and add their partial sums through distributed shared
-// memory.  Each CTA streams its rows in 64-row chunks, each chunk on its own barrier, so
-// decoding starts with the first chunk instead of after the whole slab.
+// The same product without any global workspace, for one weight (bsq_linear_dgrad) or for
+// the experts of a grouped dgrad (bsq_grouped_dgrad): the CTAs that split a column slab's
+// rows form one thread-block cluster and add their partial sums through distributed
+// shared memory.  Each CTA streams its rows in 64-row chunks, each chunk on its own
+// barrier, so decoding starts with the first chunk instead of after the whole slab.
+//
+// Grouped, every CTA builds the same list of experts that have rows for this kernel from
+// the device offsets (validated first; nothing is written when they are malformed), and
+// walks the list with stride gridDim.z.  An expert's rows go through in passes of up to
+// 16 tokens; every pass streams the expert's W slab again (from L2 after the first).
 constexpr int kChunk = 64;        // rows of W per TMA chunk (four mma k-steps)
 constexpr int kRing = 8;          // chunks in flight per CTA
 constexpr int kMaxSplits = 8;     // CTAs of a cluster (portable cluster size)
+constexpr int kTok = 16;          // token rows per pass (the mma M side)
+constexpr int kScaleStage = 128;  // FP8 scale blocks of a CTA's rows staged in shared memory
+static_assert(kMaxExperts <= 4 * kThreadsSm, "the expert scan gives each thread four experts");
 
 struct ClusterParams {
   const uint8_t* scale;
-  const float* tensor_scale;
-  __nv_bfloat16* out;
-  int32_t M, N, K;
-  int32_t rows_per_split;   // multiple of kChunk
-  int32_t scale_ld;         // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128) (1 with one scale per tensor)
-  int32_t scale_shift;      // FP8: log2 of the scale block's side (7; 31 for one scale per tensor)
-  int32_t scale_tma;        // FP4 scale windows through TMA
+  const float* tensor_scale;  // NVFP4: one per expert
+  __nv_bfloat16* out;         // bf16 [S][K]
+  const int32_t* offsets;     // cumulative end offsets [E]; null: one group of S rows
+  int64_t scale_batch;        // scale entries per expert (FP8: floats; FP4: bytes)
+  int32_t S, N, K, E;
+  int32_t rows_per_split;     // multiple of kChunk
+  int32_t scale_ld;           // MXFP4: K/32, NVFP4: K/16, FP8: ceil(K/128) (1 with one scale per tensor)
+  int32_t scale_shift;        // FP8: log2 of the scale block's side (7; 31 for one scale per tensor)
+  int32_t scale_tma;          // FP4 scale windows through TMA
+  int32_t tail_rows;          // grouped: an expert's last (rows % kTileN) rows are this kernel's when 1..tail_rows
+  int32_t drop_chunk;         // test hook: every CTA's first chunk is never copied (its wait runs out)
   uint64_t timeout_ns;
   int32_t* err;
 };
@@ -368,15 +383,31 @@ struct ClusterFmt {
   static constexpr int kRowBytes = FMT == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2;
   static constexpr int kWBytes = kChunk * kRowBytes;
   static constexpr int kSBytes = FMT == BSQ_FP8_E4M3_B128 ? 0 : kChunk * 16;
-  static constexpr int kGBytes = 16 * kChunk * 2;   // [16 tokens][64 rows] BF16, 128-byte swizzled
+  static constexpr int kGBytes = kTok * kChunk * 2;   // [16 tokens][64 rows] BF16, 128-byte swizzled
   static constexpr int kSlotBytes = kWBytes + kSBytes + kGBytes;
   static_assert(kSlotBytes % 1024 == 0, "swizzled grad_out boxes need 1024-byte aligned slots");
   static constexpr int kRingBytes = kRing * kSlotBytes;
-  static constexpr int kTreeBytes = kWarps * 16 * kSlab * 4;   // partials of the eight warps
+  static constexpr int kTreeBytes = kWarps * kTok * kSlab * 4;   // partials of the eight warps
   static constexpr int kStaged = kRingBytes > kTreeBytes ? kRingBytes : kTreeBytes;
-  static constexpr int kRedBytes = 16 * kSlab * 4;        // this CTA's partial, read by the cluster
-  static constexpr int kSmem = kStaged + kRedBytes + 256 + 1024;
+  static constexpr int kRedBytes = kTok * kSlab * 4;      // this CTA's partial, read by the cluster
+  static constexpr int kBarBytes = 256;                   // barriers, counters, status words
+  static constexpr int kScaleBytes = kScaleStage * 4;     // FP8: the pass's scales of this slab
+  static constexpr int kListBytes = kMaxExperts * 2;      // experts with rows for this kernel
+  static constexpr int kSmem = kStaged + kRedBytes + kBarBytes + kScaleBytes + kListBytes + 1024;
 };
+
+// The rows [t0, t1) of expert e that this kernel computes.
+__device__ __forceinline__ void expert_rows(const ClusterParams& p, int e, int& t0, int& t1) {
+  if (!p.offsets) {
+    t0 = 0;
+    t1 = p.S;
+    return;
+  }
+  const int r0 = e ? __ldg(p.offsets + e - 1) : 0, r1 = __ldg(p.offsets + e);
+  const int tail = (r1 - r0) % kTileN;
+  t1 = r1;
+  t0 = (tail > 0 && tail <= p.tail_rows) ? r1 - tail : r1;
+}
 
 template <int FMT>
 __global__ void __launch_bounds__(kThreadsSm, 2)
@@ -385,11 +416,16 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
   using F = ClusterFmt<FMT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* tree = reinterpret_cast<float*>(base);                  // warp partials; reuse the ring after the last chunk
+  float* tree = reinterpret_cast<float*>(base);                  // warp partials; reuse the ring after a pass
   float* red = reinterpret_cast<float*>(base + F::kStaged);      // [16 tokens][128 columns]
   uint64_t* full = reinterpret_cast<uint64_t*>(base + F::kStaged + F::kRedBytes);
-  uint64_t* empty = full + kRing;
-  int32_t* fills = reinterpret_cast<int32_t*>(empty + kRing);   // copies issued into each slot
+  uint32_t* released = reinterpret_cast<uint32_t*>(full + kRing);   // per slot: warps done with it, ever
+  int32_t* fills = reinterpret_cast<int32_t*>(released + kRing);     // copies issued into each slot
+  int32_t* pass_ok = fills + kRing;                              // this CTA's pass went through (read by the cluster)
+  int32_t* n_items = pass_ok + 1;
+  int32_t* warp_sum = n_items + 1;                               // [kWarps] scan of the expert list
+  float* scale_s = reinterpret_cast<float*>(base + F::kStaged + F::kRedBytes + F::kBarBytes);
+  int16_t* items = reinterpret_cast<int16_t*>(base + F::kStaged + F::kRedBytes + F::kBarBytes + F::kScaleBytes);
   const int slab = blockIdx.x;
   const int cb = slab * kSlab;
   const int n0 = blockIdx.y * p.rows_per_split;
@@ -402,253 +438,354 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
   const uint32_t crank = cluster_ctarank();
   const uint32_t csize = gridDim.y;  // the cluster spans the row splits of one slab
 
-  auto slot_of = [&](int c) { return base + (c % kRing) * F::kSlotBytes; };
-  auto issue = [&](int c) {          // TMA of chunk c into its ring slot
-    uint8_t* s = slot_of(c);
-    fills[c % kRing] += 1;
-    const uint32_t bar = smem_u32(&full[c % kRing]);
-    const int row = n0 + c * kChunk;
-    mbar_arrive_expect_tx(bar, F::kWBytes + ((F::kSBytes && p.scale_tma) ? F::kSBytes : 0) + F::kGBytes);
-    tma_load_2d(smem_u32(s), &tm_w, bar, FMT == BSQ_FP8_E4M3_B128 ? cb : cb / 2, row);
-    if (F::kSBytes && p.scale_tma)
-      tma_load_2d(smem_u32(s + F::kWBytes), &tm_s, bar, (FMT == BSQ_MXFP4 ? (cb >> 5) : (cb >> 4)) & ~15, row);
-    tma_load_2d(smem_u32(s + F::kWBytes + F::kSBytes), &tm_g, bar, row, 0);
-  };
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 4);   // the four warps of the chunk's group
+      released[s] = 0;
       fills[s] = 0;
     }
     fence_mbar_init();
   }
-  __syncthreads();
-  if (tid == 0)
-    for (int c = 0; c < min(nchunks, kRing); ++c) issue(c);
-
-  float tscale = 0.f;
-  if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale);
-  const int col = cb + 16 * g;
-  const bool col_ok = col < p.K;
-  float acc[kNT][4];
+  // The experts with rows here, in increasing order (the same list in every CTA).
+  if (p.offsets) {
+    int bad = 0, cnt = 0;
+    uint32_t has = 0;
 #pragma unroll
-  for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-  bool ok = true;
-  for (int c = grp; c < nchunks; c += 2) {
-    const int si = c % kRing;
-    const uint32_t par = (c / kRing) & 1u;
-    {
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait_sleep(smem_u32(&full[si]), par, 20000u)) {
-        if (global_timer_ns() - t0 > p.timeout_ns) {
-          ok = false;
-          break;
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * tid + j;
+      if (e < p.E) {
+        const int r0 = e ? __ldg(p.offsets + e - 1) : 0, r1 = __ldg(p.offsets + e);
+        if (r1 < r0 || r1 > p.S || r0 < 0) bad = 1;
+        const int tail = (r1 - r0) % kTileN;
+        if (tail > 0 && tail <= p.tail_rows) {
+          has |= 1u << j;
+          ++cnt;
         }
       }
     }
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    const uint8_t* ws_w = slot_of(c);
-    const uint8_t* ws_s = ws_w + F::kWBytes;
-    const uint32_t gb = smem_u32(ws_w + F::kWBytes + F::kSBytes);
-    const int lr = kstep * kStep;                 // the k-step's first row inside the chunk
-    const int grow0 = n0 + c * kChunk + lr;       // its row of W
-    const int rows[4] = {lr + 2 * q, lr + 2 * q + 1, lr + 8 + 2 * q, lr + 9 + 2 * q};
-    // A fragment: grad_out[token][k], k = the k-step's 16 rows (chunk lr/8, lr/8 + 1 of the
-    // 128-byte swizzled [16 tokens][64 rows] box)
-    const uint32_t c0 = static_cast<uint32_t>(((lr >> 3) ^ (g & 7)) << 4);
-    const uint32_t c1 = static_cast<uint32_t>((((lr >> 3) + 1) ^ (g & 7)) << 4);
-    uint32_t a[4];
-    a[0] = lds_u32(gb + g * 128 + c0 + 4 * q);
-    a[1] = lds_u32(gb + (g + 8) * 128 + c0 + 4 * q);
-    a[2] = lds_u32(gb + g * 128 + c1 + 4 * q);
-    a[3] = lds_u32(gb + (g + 8) * 128 + c1 + 4 * q);
-    if (FMT == BSQ_FP8_E4M3_B128) {
-      float sf = 0.f;
-      if (col_ok && grow0 < n1)
-        sf = __ldg(reinterpret_cast<const float*>(p.scale) + static_cast<int64_t>(grow0 >> p.scale_shift) * p.scale_ld +
-                   (col >> p.scale_shift));
-      const ScaleBf16 sc = make_scale_fp8(sf);   // one scale block holds the whole k-step
-      uint4 w[4];
+    if (__syncthreads_or(bad)) {
+      // every CTA of the grid reads the same offsets and leaves here, before any copy
+      if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        atomicCAS(p.err, 0, BSQ_DEVERR_BAD_OFFSETS);
+      return;
+    }
+    int incl = cnt;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(ws_w + rows[i] * F::kRowBytes + 16 * g);
-      const bool any_nan = e4m3_any_nan(w[0].x | w[0].y | w[0].z | w[0].w | w[1].x | w[1].y | w[1].z | w[1].w |
-                                        w[2].x | w[2].y | w[2].z | w[2].w | w[3].x | w[3].y | w[3].z | w[3].w);
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    int pos = incl - cnt;
+    for (int w2 = 0; w2 < warp; ++w2) pos += warp_sum[w2];
+    if (tid == kThreadsSm - 1) *n_items = pos + cnt;
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        uint32_t b0[4], b1[4];
+    for (int j = 0; j < 4; ++j)
+      if ((has >> j) & 1u) items[pos++] = static_cast<int16_t>(4 * tid + j);
+  } else if (tid == 0) {
+    *n_items = 1;
+    items[0] = 0;
+  }
+  __syncthreads();
+  const int num_items = *n_items;
+
+  auto slot_of = [&](uint32_t cc) { return base + (cc % kRing) * F::kSlotBytes; };
+  // TMA of the pass's chunk c (ring position cc) of expert e, token rows from r0
+  auto issue = [&](uint32_t cc, int c, int e, int r0) {
+    if (p.drop_chunk && cc == 0) return;
+    uint8_t* s = slot_of(cc);
+    fills[cc % kRing] += 1;
+    const uint32_t bar = smem_u32(&full[cc % kRing]);
+    const int row = n0 + c * kChunk;
+    mbar_arrive_expect_tx(bar, F::kWBytes + ((F::kSBytes && p.scale_tma) ? F::kSBytes : 0) + F::kGBytes);
+    tma_load_3d(smem_u32(s), &tm_w, bar, FMT == BSQ_FP8_E4M3_B128 ? cb : cb / 2, row, e);
+    if (F::kSBytes && p.scale_tma)
+      tma_load_3d(smem_u32(s + F::kWBytes), &tm_s, bar, (FMT == BSQ_MXFP4 ? (cb >> 5) : (cb >> 4)) & ~15, row, e);
+    tma_load_2d(smem_u32(s + F::kWBytes + F::kSBytes), &tm_g, bar, row, r0);
+  };
+
+  const int col = cb + 16 * g;
+  const bool col_ok = col < p.K;
+  uint32_t cbase = 0;    // ring position of the pass's first chunk
+  bool live = true;      // every pass so far went through in every CTA of the cluster
+  for (int it = blockIdx.z; it < num_items && live; it += gridDim.z) {
+    const int e = items[it];
+    int t0, t1;
+    expert_rows(p, e, t0, t1);
+    float tscale = 0.f;
+    if (FMT == BSQ_NVFP4) tscale = __ldg(p.tensor_scale + e);
+    const uint8_t* scale_e = p.scale + p.scale_batch * e * (FMT == BSQ_FP8_E4M3_B128 ? 4 : 1);
+    // FP8: this slab's scales of the CTA's rows, one per scale block (one per tensor: one)
+    const int sb0 = n0 >> p.scale_shift;
+    const int nsb = n1 > n0 ? ((n1 - 1) >> p.scale_shift) - sb0 + 1 : 0;
+    const bool staged = FMT == BSQ_FP8_E4M3_B128 && nsb <= kScaleStage;
+    if (staged) {
+      const float* sc = reinterpret_cast<const float*>(scale_e);
+      for (int i = tid; i < nsb; i += kThreadsSm)
+        scale_s[i] = __ldg(sc + static_cast<int64_t>(sb0 + i) * p.scale_ld + (cb >> p.scale_shift));
+      __syncthreads();
+    }
+    for (int r0 = t0; r0 < t1 && live; r0 += kTok) {
+      const int mt = min(kTok, t1 - r0);
+      if (tid == 0)
+        for (int c = 0; c < min(nchunks, kRing); ++c) issue(cbase + c, c, e, r0);
+      float acc[kNT][4];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
-          const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
-          uint32_t(&dst)[4] = half ? b1 : b0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // byte j of both rows, each in the low byte of its 16-bit half with a sign-filled
-            // byte above it; a 4-bit shift puts the magnitude bits on BF16 bits 10..4 and the
-            // sign on bit 15 (code value x 2^-120)
-            const uint32_t v = prmt(xw[wi], yw[wi], static_cast<uint32_t>(j | ((j | 8) << 4) | ((4 + j) << 8) |
-                                                                              (((4 + j) | 8) << 12)));
-            dst[j] = (v << 4) & 0x87F087F0u;
-          }
-        }
-        if (sc.fast) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            b0[j] = bf16x2_mul(b0[j], sc.c2);
-            b1[j] = bf16x2_mul(b1[j], sc.c2);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            b0[j] = bf16x2_mul(bf16x2_mul(b0[j], kPow2_120x2), sc.s2);
-            b1[j] = bf16x2_mul(bf16x2_mul(b1[j], kPow2_120x2), sc.s2);
-          }
-        }
-        if (any_nan) {
-          // S.1111.111 is NaN in E4M3; the bit move above does not see it
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
-            const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
-            uint32_t(&dst)[4] = half ? b1 : b0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (((xw[wi] >> (8 * j)) & 0x7Fu) == 0x7Fu) dst[j] = (dst[j] & 0xFFFF0000u) | kBf16NaN;
-              if (((yw[wi] >> (8 * j)) & 0x7Fu) == 0x7Fu) dst[j] = (dst[j] & 0xFFFFu) | (kBf16NaN << 16);
+      for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+      bool ok = true;
+      for (int c = grp; c < nchunks; c += 2) {
+        const uint32_t cc = cbase + c;
+        const uint32_t si = cc % kRing;
+        const uint32_t par = (cc / kRing) & 1u;
+        if (!mbar_try_wait(smem_u32(&full[si]), par)) {
+          const uint64_t w0 = global_timer_ns();
+          while (!mbar_try_wait_sleep(smem_u32(&full[si]), par, 20000u)) {
+            if (global_timer_ns() - w0 > p.timeout_ns) {
+              ok = false;
+              break;
             }
           }
         }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint8_t* ws_w = slot_of(cc);
+        const uint8_t* ws_s = ws_w + F::kWBytes;
+        const uint32_t gb = smem_u32(ws_w + F::kWBytes + F::kSBytes);
+        const int lr = kstep * kStep;                 // the k-step's first row inside the chunk
+        const int grow0 = n0 + c * kChunk + lr;       // its row of W
+        // A fragment: grad_out[token][k], k = the k-step's 16 rows (chunk lr/8, lr/8 + 1 of the
+        // 128-byte swizzled [16 tokens][64 rows] box)
+        const uint32_t c0 = static_cast<uint32_t>(((lr >> 3) ^ (g & 7)) << 4);
+        const uint32_t c1 = static_cast<uint32_t>((((lr >> 3) + 1) ^ (g & 7)) << 4);
+        uint32_t a[4];
+        a[0] = lds_u32(gb + g * 128 + c0 + 4 * q);
+        a[1] = lds_u32(gb + (g + 8) * 128 + c0 + 4 * q);
+        a[2] = lds_u32(gb + g * 128 + c1 + 4 * q);
+        a[3] = lds_u32(gb + (g + 8) * 128 + c1 + 4 * q);
+        if (FMT == BSQ_FP8_E4M3_B128) {
+          float sf;
+          if (staged) {
+            sf = scale_s[min((grow0 >> p.scale_shift) - sb0, nsb - 1)];
+          } else {
+            sf = 0.f;
+            if (col_ok && grow0 < n1)
+              sf = __ldg(reinterpret_cast<const float*>(scale_e) + static_cast<int64_t>(grow0 >> p.scale_shift) * p.scale_ld +
+                         (col >> p.scale_shift));
+          }
+          const ScaleBf16 sc = make_scale_fp8(sf);   // one scale block holds the whole k-step
+          // rows lr+2q, lr+2q+1, lr+8+2q, lr+9+2q, 16 codes each from column 16g: 16-byte
+          // chunk g of a 128-byte row, stored at chunk g ^ (row & 7) (128-byte swizzle)
+          uint4 w[4];
+          const uint32_t wrow = smem_u32(ws_w) + static_cast<uint32_t>(lr + 2 * q) * F::kRowBytes;
+          w[0] = lds128(wrow + ((g ^ (2 * q)) << 4));
+          w[1] = lds128(wrow + F::kRowBytes + ((g ^ (2 * q + 1)) << 4));
+          w[2] = lds128(wrow + 8 * F::kRowBytes + ((g ^ (2 * q)) << 4));
+          w[3] = lds128(wrow + 9 * F::kRowBytes + ((g ^ (2 * q + 1)) << 4));
+          const bool any_nan = e4m3_marked(
+              e4m3_nan_mark(w[0].x) | e4m3_nan_mark(w[0].y) | e4m3_nan_mark(w[0].z) | e4m3_nan_mark(w[0].w) |
+              e4m3_nan_mark(w[1].x) | e4m3_nan_mark(w[1].y) | e4m3_nan_mark(w[1].z) | e4m3_nan_mark(w[1].w) |
+              e4m3_nan_mark(w[2].x) | e4m3_nan_mark(w[2].y) | e4m3_nan_mark(w[2].z) | e4m3_nan_mark(w[2].w) |
+              e4m3_nan_mark(w[3].x) | e4m3_nan_mark(w[3].y) | e4m3_nan_mark(w[3].z) | e4m3_nan_mark(w[3].w));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mma_bf16_16816(acc[4 * wi + j], a, b0[j], b1[j]);
-      }
-    } else {
-      uint2 w[4];
-      uint32_t sraw[4];
+          for (int wi = 0; wi < 4; ++wi) {
+            uint32_t b0[4], b1[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w[i] = *reinterpret_cast<const uint2*>(ws_w + rows[i] * F::kRowBytes + 8 * g);
-        const int grow = n0 + c * kChunk + rows[i];
-        if (p.scale_tma) {
-          sraw[i] = FMT == BSQ_MXFP4 ? ws_s[rows[i] * 16 + ((cb >> 5) & 15) + (g >> 1)]
-                                     : ws_s[rows[i] * 16 + ((cb >> 4) & 15) + g];
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+              const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+              uint32_t(&dst)[4] = half ? b1 : b0;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                // byte j of both rows, each in the low byte of its 16-bit half with a sign-filled
+                // byte above it; a 4-bit shift puts the magnitude bits on BF16 bits 10..4 and the
+                // sign on bit 15 (code value x 2^-120)
+                const uint32_t v = prmt(xw[wi], yw[wi], static_cast<uint32_t>(j | ((j | 8) << 4) | ((4 + j) << 8) |
+                                                                                  (((4 + j) | 8) << 12)));
+                dst[j] = (v << 4) & 0x87F087F0u;
+              }
+            }
+            if (sc.fast) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                b0[j] = bf16x2_mul(b0[j], sc.c2);
+                b1[j] = bf16x2_mul(b1[j], sc.c2);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                b0[j] = bf16x2_mul(bf16x2_mul(b0[j], kPow2_120x2), sc.s2);
+                b1[j] = bf16x2_mul(bf16x2_mul(b1[j], kPow2_120x2), sc.s2);
+              }
+            }
+            if (any_nan) {
+              // S.1111.111 is NaN in E4M3; the bit move above does not see it
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+                const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+                uint32_t(&dst)[4] = half ? b1 : b0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  if (((xw[wi] >> (8 * j)) & 0x7Fu) == 0x7Fu) dst[j] = (dst[j] & 0xFFFF0000u) | kBf16NaN;
+                  if (((yw[wi] >> (8 * j)) & 0x7Fu) == 0x7Fu) dst[j] = (dst[j] & 0xFFFFu) | (kBf16NaN << 16);
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mma_bf16_16816(acc[4 * wi + j], a, b0[j], b1[j]);
+          }
         } else {
-          sraw[i] = 0;
-          if (col_ok && grow < n1)
-            sraw[i] = __ldg(p.scale + static_cast<int64_t>(grow) * p.scale_ld + (FMT == BSQ_MXFP4 ? (col >> 5) : (col >> 4)));
-        }
-      }
-      // the scales of the k-step's four rows (rows 2q, 2q+1 pair in b0, rows 8+2q, 9+2q in b1)
-      const ScaleBf16 sc0 = pair_scales(row_scale<FMT>(sraw[0], tscale), row_scale<FMT>(sraw[1], tscale));
-      const ScaleBf16 sc1 = pair_scales(row_scale<FMT>(sraw[2], tscale), row_scale<FMT>(sraw[3], tscale));
-      const bool fast = sc0.fast && sc1.fast;
+          // rows lr+2q, lr+2q+1, lr+8+2q, lr+9+2q, 8 bytes each from byte 8g: 16-byte chunk
+          // g/2 of a 64-byte row, stored at chunk (g/2) ^ ((row >> 1) & 3) = (g/2) ^ q
+          // (64-byte swizzle).  Lanes with odd q load the odd row first, so that the 16
+          // lanes of each access phase cover all 32 banks once.
+          const int rows[4] = {lr + 2 * q, lr + 2 * q + 1, lr + 8 + 2 * q, lr + 9 + 2 * q};
+          const uint32_t wbase = smem_u32(ws_w) + static_cast<uint32_t>((((g >> 1) ^ q) << 4) + 8 * (g & 1));
+          const int odd = q & 1;
+          uint2 w[4];
+          {
+            const uint32_t ra = wbase + static_cast<uint32_t>(lr + 2 * q + odd) * F::kRowBytes;       // first
+            const uint32_t rb = wbase + static_cast<uint32_t>(lr + 2 * q + 1 - odd) * F::kRowBytes;   // second
+            const uint2 x0 = lds_u64(ra);
+            const uint2 x1 = lds_u64(rb);
+            const uint2 x2 = lds_u64(ra + 8 * F::kRowBytes);
+            const uint2 x3 = lds_u64(rb + 8 * F::kRowBytes);
+            w[0] = odd ? x1 : x0;
+            w[1] = odd ? x0 : x1;
+            w[2] = odd ? x3 : x2;
+            w[3] = odd ? x2 : x3;
+          }
+          uint32_t sraw[4];
 #pragma unroll
-      for (int wi = 0; wi < 2; ++wi) {
-        uint32_t b0[8], b1[8];
+          for (int i = 0; i < 4; ++i) {
+            const int grow = n0 + c * kChunk + rows[i];
+            if (p.scale_tma) {
+              sraw[i] = FMT == BSQ_MXFP4 ? ws_s[rows[i] * 16 + ((cb >> 5) & 15) + (g >> 1)]
+                                         : ws_s[rows[i] * 16 + ((cb >> 4) & 15) + g];
+            } else {
+              sraw[i] = 0;
+              if (col_ok && grow < n1)
+                sraw[i] = __ldg(scale_e + static_cast<int64_t>(grow) * p.scale_ld + (FMT == BSQ_MXFP4 ? (col >> 5) : (col >> 4)));
+            }
+          }
+          // the scales of the k-step's four rows (rows 2q, 2q+1 pair in b0, rows 8+2q, 9+2q in b1)
+          const ScaleBf16 sc0 = pair_scales(row_scale<FMT>(sraw[0], tscale), row_scale<FMT>(sraw[1], tscale));
+          const ScaleBf16 sc1 = pair_scales(row_scale<FMT>(sraw[2], tscale), row_scale<FMT>(sraw[3], tscale));
+          const bool fast = sc0.fast && sc1.fast;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
-          const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
-          uint32_t(&dst)[8] = half ? b1 : b0;
+          for (int wi = 0; wi < 2; ++wi) {
+            uint32_t b0[8], b1[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t v = pair_bytes(xw[wi], yw[wi], j);                // byte 4wi+j of both rows
-            dst[2 * j] = ((v & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;         // column 8wi+2j
-            dst[2 * j + 1] = ((v & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;     // column 8wi+2j+1
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t* xw = reinterpret_cast<const uint32_t*>(&w[2 * half]);
+              const uint32_t* yw = reinterpret_cast<const uint32_t*>(&w[2 * half + 1]);
+              uint32_t(&dst)[8] = half ? b1 : b0;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t v = pair_bytes(xw[wi], yw[wi], j);                // byte 4wi+j of both rows
+                dst[2 * j] = ((v & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;         // column 8wi+2j
+                dst[2 * j + 1] = ((v & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;     // column 8wi+2j+1
+              }
+            }
+            if (fast) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                b0[j] = bf16x2_mul(b0[j], sc0.c2);
+                b1[j] = bf16x2_mul(b1[j], sc1.c2);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                b0[j] = scale_one(b0[j], sc0, kPow2_126x2);
+                b1[j] = scale_one(b1[j], sc1, kPow2_126x2);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mma_bf16_16816(acc[8 * wi + j], a, b0[j], b1[j]);
           }
         }
-        if (fast) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            b0[j] = bf16x2_mul(b0[j], sc0.c2);
-            b1[j] = bf16x2_mul(b1[j], sc1.c2);
+        // This warp is done with the chunk's slot (its reads are in registers and consumed).
+        // The fourth warp of the group to let it go refills it with the chunk kRing later:
+        // nobody waits for a slot to drain.
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          const uint32_t prior = atomicAdd(&released[si], 1u);
+          if ((prior & 3u) == 3u && c + kRing < nchunks) {
+            __threadfence_block();
+            fence_proxy_async_smem();   // the slot's plain reads come before the copy that overwrites it
+            issue(cc + kRing, c + kRing, e, r0);
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            b0[j] = scale_one(b0[j], sc0, kPow2_126x2);
-            b1[j] = scale_one(b1[j], sc1, kPow2_126x2);
+        }
+      }
+      // One decision for the CTA; after a timeout the CTA writes nothing, lets its copies in
+      // flight land and still meets its cluster at both barriers.
+      ok = __syncthreads_and(ok) != 0;
+      if (!ok) {
+        if (tid == 0) {
+          atomicCAS(p.err, 0, BSQ_DEVERR_TIMEOUT);
+          // the last fill of every slot (slot fills are issued in order)
+          for (int s = 0; s < kRing; ++s) {
+            if (fills[s] == 0) continue;
+            const uint64_t w0 = global_timer_ns();
+            while (!mbar_try_wait(smem_u32(&full[s]), (fills[s] - 1) & 1) && global_timer_ns() - w0 < kDrainLimitNs) {
+            }
           }
         }
+        __syncthreads();
+      } else {
+        // Every warp stores its partial through the idle ring, fragment by fragment
+        // ([warp][n-tile][fragment register][lane], conflict-free); then every thread adds the
+        // eight warps' values of its entries and writes the CTA's partial red[token][column]
+        // (column = 16 n + n-tile of the slab).
+        {
+          float* dst = tree + warp * (kNT * 4 * 32);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mma_bf16_16816(acc[8 * wi + j], a, b0[j], b1[j]);
-      }
-    }
-    // this warp is done with the chunk's slot; the group's first warp refills it with the
-    // chunk kRing later once all four have let it go
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[si]));
-    if (kstep == 0 && lane == 0 && c + kRing < nchunks) {
-      const uint64_t t0 = global_timer_ns();
-      bool freed = true;
-      while (!mbar_try_wait(smem_u32(&empty[si]), par)) {
-        if (global_timer_ns() - t0 > p.timeout_ns) {
-          freed = false;
-          break;
+          for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) dst[(nt * 4 + r) * 32 + lane] = acc[nt][r];
+        }
+        __syncthreads();
+        for (int i = tid; i < kNT * 4 * 32; i += kThreadsSm) {
+          float v = 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < kWarps; ++w2) v += tree[w2 * (kNT * 4 * 32) + i];
+          const int l = i & 31, rr = (i >> 5) & 3, nt = i >> 7;
+          const int t = (l >> 2) + ((rr & 2) ? 8 : 0), n = 2 * (l & 3) + (rr & 1);
+          red[t * kSlab + 16 * n + nt] = v;
         }
       }
-      if (freed) issue(c + kRing);
-      else ok = false;
-    }
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-  }
-  // One decision for the CTA; after a timeout the CTA writes nothing but still meets its
-  // cluster at both barriers (its peers read its partial, which is then undefined).
-  ok = __syncthreads_and(ok) != 0;
-  if (!ok) {
-    if (tid == 0) {
-      atomicCAS(p.err, 0, BSQ_DEVERR_TIMEOUT);
-      // let the copies still in flight land before the shared memory is reused or freed:
-      // the last fill of every slot (slot fills are issued in order)
-      for (int s = 0; s < kRing; ++s) {
-        if (fills[s] == 0) continue;
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(smem_u32(&full[s]), (fills[s] - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+      if (tid == 0) *pass_ok = ok ? 1 : 0;
+      // Every partial of the cluster and its status are in place (release/acquire at cluster scope) ...
+      cluster_sync();
+      {
+        uint32_t peer_ok = 1u;
+        if (static_cast<uint32_t>(lane) < csize) peer_ok = ld_shared_cluster_u32(map_to_rank(smem_u32(pass_ok), lane));
+        live = __all_sync(0xffffffffu, peer_ok != 0u);
+      }
+      // ... and CTA r of the cluster adds columns [r*cw, (r+1)*cw) of the slab over all of them.
+      const int cw = ((kSlab + static_cast<int>(csize) - 1) / static_cast<int>(csize) + 3) & ~3;
+      const int c_lo = static_cast<int>(crank) * cw, c_hi = min(kSlab, c_lo + cw);
+      if (live && c_hi > c_lo) {
+        const int span = c_hi - c_lo;
+        for (int i = tid; i < mt * span; i += kThreadsSm) {
+          const int t = i / span, cc = c_lo + i % span;
+          const uint32_t off = smem_u32(red + t * kSlab + cc);
+          float v = 0.f;
+          for (uint32_t r = 0; r < csize; ++r) v += ld_shared_cluster_f32(map_to_rank(off, r));
+          if (cb + cc < p.K) p.out[static_cast<int64_t>(r0 + t) * p.K + cb + cc] = __float2bfloat16_rn(v);
         }
       }
-    }
-    __syncthreads();
-  } else {
-    // Every warp stores its partial through the idle ring, fragment by fragment
-    // ([warp][n-tile][fragment register][lane], conflict-free); then every thread adds the
-    // eight warps' values of its entries and writes the CTA's partial red[token][column]
-    // (column = 16 n + n-tile of the slab).
-    {
-      float* dst = tree + warp * (kNT * 4 * 32);
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) dst[(nt * 4 + r) * 32 + lane] = acc[nt][r];
-    }
-    __syncthreads();
-    for (int e = tid; e < kNT * 4 * 32; e += kThreadsSm) {
-      float v = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < kWarps; ++w2) v += tree[w2 * (kNT * 4 * 32) + e];
-      const int l = e & 31, rr = (e >> 5) & 3, nt = e >> 7;
-      const int t = (l >> 2) + ((rr & 2) ? 8 : 0), n = 2 * (l & 3) + (rr & 1);
-      red[t * kSlab + 16 * n + nt] = v;
+      // The ring was written as plain shared memory (the warp partials); the next pass's
+      // copies write it through the async proxy.
+      fence_proxy_async_smem();
+      // No CTA goes on (or leaves) while its peers may still read its partial.
+      cluster_sync();
+      cbase += static_cast<uint32_t>(nchunks);
     }
   }
-  // Every partial of the cluster is in place (release/acquire at cluster scope) ...
-  cluster_sync();
-  // ... and CTA r of the cluster adds columns [r*cw, (r+1)*cw) of the slab over all of them.
-  const int cw = ((kSlab + static_cast<int>(csize) - 1) / static_cast<int>(csize) + 3) & ~3;
-  const int c_lo = static_cast<int>(crank) * cw, c_hi = min(kSlab, c_lo + cw);
-  if (ok && c_hi > c_lo) {
-    const int span = c_hi - c_lo;
-    for (int i = tid; i < p.M * span; i += kThreadsSm) {
-      const int t = i / span, cc = c_lo + i % span;
-      const uint32_t off = smem_u32(red + t * kSlab + cc);
-      float v = 0.f;
-      for (uint32_t r = 0; r < csize; ++r) v += ld_shared_cluster_f32(map_to_rank(off, r));
-      if (cb + cc < p.K) p.out[static_cast<int64_t>(t) * p.K + cb + cc] = __float2bfloat16_rn(v);
-    }
-  }
-  // No CTA leaves while its peers may still read its partial.
-  cluster_sync();
 }
 
 }  // namespace
@@ -747,41 +884,76 @@ int launch_smallm(const SmallMArgs& a, const char** msg) {
   return 0;
 }
 
+namespace {
+int env_rows(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  const long r = std::strtol(v, nullptr, 10);
+  return r < 0 ? 0 : (r > kTileN - 1 ? kTileN - 1 : static_cast<int>(r));
+}
+}  // namespace
+
+int grouped_small_rows() { return env_rows("BSQ_GROUPED_SMALL_ROWS", kGroupedSmallRows); }
+int grouped_tail_rows() { return env_rows("BSQ_GROUPED_TAIL_ROWS", 0); }
+
 int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   const int fmt = kernel_fmt(a.fmt);
+  const bool grouped = a.offsets != nullptr;
   ClusterParams p;
   p.scale = static_cast<const uint8_t*>(a.w_scale);
   p.tensor_scale = a.w_tensor_scale;
   p.out = static_cast<__nv_bfloat16*>(a.out);
-  p.M = static_cast<int32_t>(a.M);
+  p.offsets = a.offsets;
+  p.S = static_cast<int32_t>(a.M);
   p.N = static_cast<int32_t>(a.N);
   p.K = static_cast<int32_t>(a.K);
+  p.E = grouped ? static_cast<int32_t>(a.E) : 1;
+  p.tail_rows = grouped ? a.tail_rows : 0;
   p.err = a.err;
   p.timeout_ns = wait_limit_ns();
+  // Test hook (failure detection without a GPU fault): with BSQ_TEST_DROP_CHUNK=1 the first
+  // chunk of every CTA is never requested, so the wait for it runs out and the kernel takes
+  // its orderly abort.
+  const char* drop = std::getenv("BSQ_TEST_DROP_CHUNK");
+  p.drop_chunk = drop && drop[0] == '1' ? 1 : 0;
+  const bool per_tensor = a.fmt == BSQ_FP8_E4M3_TENSOR;
   p.scale_ld = fmt == BSQ_MXFP4 ? static_cast<int32_t>(a.K / 32)
                : fmt == BSQ_NVFP4 ? static_cast<int32_t>(a.K / 16)
-               : a.fmt == BSQ_FP8_E4M3_TENSOR ? 1
+               : per_tensor       ? 1
                                   : static_cast<int32_t>((a.K + 127) / 128);
+  p.scale_batch = fmt == BSQ_FP8_E4M3_B128 ? (per_tensor ? 1 : ((a.N + 127) / 128) * p.scale_ld) : a.N * p.scale_ld;
   p.scale_shift = fp8_scale_shift(a.fmt);
   const int slabs = static_cast<int>((a.K + kSlab - 1) / kSlab);
+  // Experts walked at once (grid z): every one that can have rows here when the whole
+  // grouped product is this kernel's (S within tail_rows), else an estimate of how many
+  // ragged last tiles fall within tail_rows; a CTA takes further experts in turn.
+  int64_t gz = 1;
+  if (grouped) {
+    gz = a.M <= a.tail_rows ? std::min<int64_t>(a.E, a.M) : (a.E * a.tail_rows + kTileN - 1) / kTileN;
+    gz = std::max<int64_t>(1, std::min<int64_t>(gz, std::min<int64_t>(a.E, a.M)));
+  }
   // Row splits = the cluster size: about two CTAs per SM in one wave, at most 8, and no
   // more splits than 64-row chunks.
-  int splits = (2 * a.num_sms) / slabs;
+  int64_t splits = (2 * a.num_sms) / (slabs * gz);
   const int64_t max_by_rows = (a.N + kChunk - 1) / kChunk;
   if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits > max_by_rows) splits = static_cast<int>(max_by_rows);
+  if (splits > max_by_rows) splits = max_by_rows;
   if (splits < 1) splits = 1;
   int64_t rps = (a.N + splits - 1) / splits;
   rps = (rps + kChunk - 1) / kChunk * kChunk;
   p.rows_per_split = static_cast<int32_t>(rps);
+  const uint64_t batch = static_cast<uint64_t>(p.E);
   CUtensorMap tm_w, tm_s, tm_g;
   const uint64_t wrow = fmt == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
   {
-    const uint64_t dims[2] = {wrow, static_cast<uint64_t>(a.N)};
-    const uint64_t strides[1] = {wrow};
-    const uint32_t box[2] = {static_cast<uint32_t>(fmt == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2),
-                             static_cast<uint32_t>(kChunk)};
-    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    const uint64_t dims[3] = {wrow, static_cast<uint64_t>(a.N), batch};
+    const uint64_t strides[2] = {wrow, wrow * static_cast<uint64_t>(a.N)};
+    const uint32_t box[3] = {static_cast<uint32_t>(fmt == BSQ_FP8_E4M3_B128 ? kSlab : kSlab / 2),
+                             static_cast<uint32_t>(kChunk), 1};
+    // rows of 128 (FP8) or 64 (FP4) bytes, swizzled so that the decode's reads are free of
+    // bank conflicts
+    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w_data, dims, strides, box,
+                    fmt == BSQ_FP8_E4M3_B128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
       *msg = "tensor map encoding failed for W";
       return -1;
     }
@@ -789,7 +961,7 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
-    const uint32_t box[2] = {64, 16};
+    const uint32_t box[2] = {64, kTok};
     if (!encode_map(&tm_g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
       *msg = "tensor map encoding failed for grad_out";
       return -1;
@@ -800,10 +972,10 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   if (fmt == BSQ_MXFP4 || fmt == BSQ_NVFP4) {
     const uint64_t srow = fmt == BSQ_MXFP4 ? a.K / 32 : a.K / 16;
     if (srow % 16 == 0 && (reinterpret_cast<uintptr_t>(a.w_scale) & 15u) == 0) {
-      const uint64_t dims[2] = {srow, static_cast<uint64_t>(a.N)};
-      const uint64_t strides[1] = {srow};
-      const uint32_t box[2] = {16, static_cast<uint32_t>(kChunk)};
-      if (!encode_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w_scale, dims, strides, box,
+      const uint64_t dims[3] = {srow, static_cast<uint64_t>(a.N), batch};
+      const uint64_t strides[2] = {srow, srow * static_cast<uint64_t>(a.N)};
+      const uint32_t box[3] = {16, static_cast<uint32_t>(kChunk), 1};
+      if (!encode_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w_scale, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE)) {
         *msg = "tensor map encoding failed for the scales";
         return -1;
@@ -817,7 +989,7 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = static_cast<unsigned>(splits);
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(splits));
+  cfg.gridDim = dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(splits), static_cast<unsigned>(gz));
   cfg.blockDim = dim3(kThreadsSm);
   cfg.stream = a.stream;
   cfg.attrs = attr;

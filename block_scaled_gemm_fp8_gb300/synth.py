@@ -297,7 +297,7 @@ CONFIG_NAMES = {
 }
 
 
-def make_config(n, device="cpu", seed=0, small_m=16, experts=None):
+def make_config(n, device="cpu", seed=0, small_m=16, experts=None, rows=None):
     """Inputs of workload ``n`` (1..5) on ``device``; returns a dict of tensors and sizes.
 
     Keys: ``G`` (bf16 grad_out), ``W`` (Packed, [E or 1, N, K]), ``X`` (Packed or None,
@@ -305,6 +305,8 @@ def make_config(n, device="cpu", seed=0, small_m=16, experts=None):
     workload 2 ``G_small`` (bf16 [small_m, N]).  ``experts`` (grouped workloads only)
     scales the workload down to that many experts with the same tokens per expert and
     the same routing law (a smaller case of the same kernels, e.g. for profiling).
+    ``rows`` (workload 4 only) keeps the 64 expert weights and routes that many grad_out
+    rows instead of 16384 under the same law: a decode-sized batch.
     """
     base = seed * 100
     if n == 1:
@@ -330,10 +332,13 @@ def make_config(n, device="cpu", seed=0, small_m=16, experts=None):
         E, S, N, K = 64, 16384, 2816, 2048
         if experts:
             E, S = experts, S * experts // E
+        if rows:
+            S = rows
         counts = zipf_counts(S, E, 1.1, base + 5, force_empty=[e for e in (0, 31, 63) if e < E])
         W = make_packed(FMT_FP8, E, N, K, 0.02, base + 2, device)
         G = randn((S, N), 1.0, base + 3, device, torch.bfloat16)
-        name = CONFIG_NAMES[n] if E == 64 else f"fp8_grouped_dgrad_E{E}_S{S}_N{N}_K{K}"
+        name = (f"fp8_grouped_dgrad_decode_E{E}_S{S}_N{N}_K{K}" if rows
+                else CONFIG_NAMES[n] if E == 64 else f"fp8_grouped_dgrad_E{E}_S{S}_N{N}_K{K}")
         return dict(name=name, M=S, N=N, K=K, E=E, G=G, W=W, X=None,
                     offsets=offsets_from_counts(counts), grouped=True)
     if n == 5:

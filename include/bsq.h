@@ -60,11 +60,20 @@
  *       BSQ_GEMM_SHORT_TILES  wgrad of a packed format: 1 = the short-tile GEMM kernel (more
  *                             epilogue warps), 0 = the default kernel; unset = the short-tile
  *                             kernel when the groups average fewer than 1024 rows (S < 1024*E).
+ *       BSQ_GROUPED_SMALL_ROWS grouped dgrad of a packed W with S at most this many rows
+ *                             (0..255, default 64) runs wholly in the split-K small-M kernel
+ *                             (decode-sized batches); above it the pair-tile GEMM runs.
+ *       BSQ_GROUPED_TAIL_ROWS above that bound, an expert's ragged last GEMM tile of at most
+ *                             this many rows (0..255, default 0 = none) goes to the small-M
+ *                             kernel instead; the two kernels then run one after the other.
  *       BSQ_TEST_DROP_ANNOUNCE test hook for failure detection: 1 = in the GEMM kernels, the
  *                             even CTA of each pair never announces a unit's operands, so the
  *                             MMA thread's wait runs out of time (BSQ_WAIT_LIMIT_*), the kernel
  *                             stops in order and records BSQ_DEVERR_TIMEOUT.  Never set it
  *                             outside such a test: every GEMM call then fails.
+ *       BSQ_TEST_DROP_CHUNK   the same for the small-M kernel (bsq_linear_dgrad with M <= 16,
+ *                             decode-sized bsq_grouped_dgrad): every CTA's first chunk is
+ *                             never requested, so the wait for it runs out.
  */
 #ifndef BSQ_H
 #define BSQ_H
@@ -174,8 +183,11 @@ bsq_status bsq_linear_forward(int32_t x_fmt, const void* x_data, const void* x_s
  * offsets: device int32[E], cumulative END offsets without a leading zero
  * (expert e owns rows [e ? offsets[e-1] : 0, offsets[e])), non-decreasing, offsets[E-1] <= S.
  * W: packed [E][N][K]; w_tensor_scale (NVFP4) is per expert, f32[E].
- * grad_x: bf16[S][K]; rows >= offsets[E-1] are neither read (grad_out) nor written.
+ * grad_x: bf16[S][K]; rows >= offsets[E-1] of grad_x are not written, and the values of
+ * grad_out there (possibly uninitialised) never reach a result.
  * 1 <= E <= 1024.
+ * Kernels: with S <= 64 rows in all (BSQ_GROUPED_SMALL_ROWS) the split-K small-M kernel,
+ * which reads every routed expert's packed weight once per 16 rows; else the pair-tile GEMM.
  */
 bsq_status bsq_grouped_dgrad(const void* grad_out, int64_t S, int64_t N,
                              int32_t w_fmt, const void* w_data, const void* w_scale,
