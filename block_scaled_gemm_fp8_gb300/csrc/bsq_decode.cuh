@@ -23,6 +23,8 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "../../include/bsq.h"
+
 #include "bsq_ptx.cuh"
 
 namespace bsq {
@@ -36,6 +38,16 @@ __host__ __device__ constexpr int perm_fp4(int p) { return (p & 1) ? (p >> 1) + 
 __host__ __device__ constexpr int perm_fp8(int p) {
   // (c0,c2),(c1,c3),(c4,c6),(c5,c7)
   return (p & 4) | ((p & 1) << 1) | ((p >> 1) & 1);
+}
+
+// A decoded 8-column group holds its columns in the order of the decode's BF16 pairs
+// (perm_fp4 / perm_fp8 of the position); position i of a row of such groups holds column
+// lane_to_col(i).
+template <int FMT>
+__device__ __forceinline__ int lane_to_col(int i) {
+  if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) return (i & ~7) | perm_fp4(i & 7);
+  if (FMT == BSQ_FP8_E4M3_B128) return (i & ~7) | perm_fp8(i & 7);
+  return i;
 }
 
 struct ScaleBf16 {

@@ -239,12 +239,6 @@ __device__ __forceinline__ int mma_width(bool dgrad, int n_valid, int b_mode) {
   return max(32, (n_valid + 15) & ~15);
 }
 
-template <int FMT>
-__device__ __forceinline__ int lane_to_col(int i) {
-  if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) return (i & ~7) | perm_fp4(i & 7);
-  if (FMT == BSQ_FP8_E4M3_B128) return (i & ~7) | perm_fp8(i & 7);
-  return i;
-}
 
 // This thread's 32 packed codes of one k-block row (FP8: wa = codes 0..15 as read, wb the
 // other 16; FP4: wa) -> 4 groups of 4 BF16 pairs, scaled; zeros outside the operand.

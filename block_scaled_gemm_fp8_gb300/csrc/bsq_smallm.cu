@@ -893,6 +893,66 @@ int env_rows(const char* name, int dflt) {
 }
 }  // namespace
 
+// Shared memory and its carveout for a small-M kernel (the carveout at its maximum, so
+// that two CTAs fit on an SM).
+template <typename Kern>
+static cudaError_t set_smem(Kern kern, int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+// Clusters of `size` CTAs of the small-M kernel that fit on the current device at once
+// (cudaOccupancyMaxActiveClusters), cached per device; 0 when the query fails.
+static int resident_clusters(int fmt, int size) {
+  static std::mutex mu;
+  static int table[kMaxDevices][3][kMaxSplits + 1];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int fi = fmt == BSQ_MXFP4 ? 0 : fmt == BSQ_NVFP4 ? 1 : 2;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& d : table)
+      for (auto& f : d)
+        for (int& v : f) v = -1;
+    init = true;
+  }
+  int& slot = table[dev][fi][size];
+  if (slot >= 0) return slot;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(size);
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(1, static_cast<unsigned>(size), 1);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e = cudaSuccess;
+#define BSQ_OCC(F_)                                                                                  \
+  cfg.blockDim = dim3(kThreadsSm);                                                                   \
+  cfg.dynamicSmemBytes = ClusterFmt<F_>::kSmem;                                                      \
+  e = set_smem(smallm_dgrad_cluster_kernel<F_>, ClusterFmt<F_>::kSmem);                              \
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, smallm_dgrad_cluster_kernel<F_>, &cfg);
+  if (fi == 0) {
+    BSQ_OCC(BSQ_MXFP4)
+  } else if (fi == 1) {
+    BSQ_OCC(BSQ_NVFP4)
+  } else {
+    BSQ_OCC(BSQ_FP8_E4M3_B128)
+  }
+#undef BSQ_OCC
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  slot = n;
+  return n;
+}
+
 int grouped_small_rows() { return env_rows("BSQ_GROUPED_SMALL_ROWS", kGroupedSmallRows); }
 int grouped_tail_rows() { return env_rows("BSQ_GROUPED_TAIL_ROWS", 0); }
 
@@ -932,13 +992,28 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
     gz = a.M <= a.tail_rows ? std::min<int64_t>(a.E, a.M) : (a.E * a.tail_rows + kTileN - 1) / kTileN;
     gz = std::max<int64_t>(1, std::min<int64_t>(gz, std::min<int64_t>(a.E, a.M)));
   }
-  // Row splits = the cluster size: about two CTAs per SM in one wave, at most 8, and no
-  // more splits than 64-row chunks.
-  int64_t splits = (2 * a.num_sms) / (slabs * gz);
+  // Row splits = the cluster size, at most 8 and no more than there are 64-row chunks.
+  // One weight: fewer clusters of a larger size fit on the GPU at once (a cluster's CTAs
+  // share one GPC), so the size is the one with the least time by (waves of resident
+  // clusters) x (chunks per split); ties go to fewer splits.  Grouped: most grid-z slots of
+  // a decode-sized call hold no expert and end at once, so the grid is sized as if every
+  // slot worked, about two CTAs per SM.
   const int64_t max_by_rows = (a.N + kChunk - 1) / kChunk;
-  if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits > max_by_rows) splits = max_by_rows;
-  if (splits < 1) splits = 1;
+  int64_t splits = 1, best = -1;
+  if (grouped) {
+    splits = std::max<int64_t>(1, std::min<int64_t>({(2 * a.num_sms) / (slabs * gz), kMaxSplits, max_by_rows}));
+    best = 0;
+  }
+  for (int64_t sz = 1; !grouped && sz <= std::min<int64_t>(kMaxSplits, max_by_rows); ++sz) {
+    const int act = resident_clusters(fmt, static_cast<int>(sz));
+    if (act <= 0) continue;
+    const int64_t waves = (slabs * gz + act - 1) / act;
+    const int64_t cost = waves * ((a.N + sz * kChunk - 1) / (sz * kChunk));
+    if (best < 0 || cost < best) {
+      best = cost;
+      splits = sz;
+    }
+  }
   int64_t rps = (a.N + splits - 1) / splits;
   rps = (rps + kChunk - 1) / kChunk * kChunk;
   p.rows_per_split = static_cast<int32_t>(rps);
@@ -952,8 +1027,8 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
                              static_cast<uint32_t>(kChunk), 1};
     // rows of 128 (FP8) or 64 (FP4) bytes, swizzled so that the decode's reads are free of
     // bank conflicts
-    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w_data, dims, strides, box,
-                    fmt == BSQ_FP8_E4M3_B128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)) {
+    const CUtensorMapSwizzle sw = fmt == BSQ_FP8_E4M3_B128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w_data, dims, strides, box, sw)) {
       *msg = "tensor map encoding failed for W";
       return -1;
     }
@@ -997,8 +1072,7 @@ int launch_smallm_cluster(const SmallMArgs& a, const char** msg) {
   cudaError_t e = cudaSuccess;
 #define BSQ_LAUNCH_CLUSTER(F_)                                                                                       \
   cfg.dynamicSmemBytes = ClusterFmt<F_>::kSmem;                                                                     \
-  e = cudaFuncSetAttribute(smallm_dgrad_cluster_kernel<F_>, cudaFuncAttributeMaxDynamicSharedMemorySize,           \
-                           ClusterFmt<F_>::kSmem);                                                                  \
+  e = set_smem(smallm_dgrad_cluster_kernel<F_>, ClusterFmt<F_>::kSmem);                                             \
   if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, smallm_dgrad_cluster_kernel<F_>, tm_w, tm_s, tm_g, p);
   switch (fmt) {
     case BSQ_MXFP4: BSQ_LAUNCH_CLUSTER(BSQ_MXFP4) break;
