@@ -13,6 +13,8 @@ significant bits and a BF16 scale at most 8) and rounded once, to nearest even.
     `block_size is None` branch -- the scale, cast to the gradient dtype, is
     broadcast over the weight without repetition; for a grouped weight [E, N, K]
     there is one scale per expert.
+  * FP8 E5M2 with one float32 quantization step per tensor: the gradient of AstrAI
+    fp8.py's "hybrid" backward (quantize.py), dequantized by the same rule.
   * MXFP4 (E2M1 codes, two per byte, one E8M0 scale per 32 consecutive elements
     of a row) and NVFP4 (E2M1 codes, one E4M3 scale per 16 consecutive elements
     of a row, one float32 scale per tensor): MSLK PR #393, "Implementation
@@ -30,12 +32,13 @@ Shapes: every tensor is [batch, rows, cols] with cols the contiguous axis.
 
 import numpy as np
 
-from .formats import (E2M1_TABLE, E4M3_TABLE, E8M0_TABLE, bf16_bits, bf16_round,
+from .formats import (E2M1_TABLE, E4M3_TABLE, E5M2_TABLE, E8M0_TABLE, bf16_bits, bf16_round,
                       fp32_round)
 
 FMT_BF16 = "bf16"
 FMT_FP8 = "fp8_e4m3_b128"
 FMT_FP8_TENSOR = "fp8_e4m3_tensor"
+FMT_E5M2_TENSOR = "fp8_e5m2_tensor"
 FMT_MXFP4 = "mxfp4"
 FMT_NVFP4 = "nvfp4"
 
@@ -61,7 +64,7 @@ def scale_values(fmt, scale, tensor_scale, batch, rows, cols):
         ri = np.arange(rows) // FP8_BLOCK
         ci = np.arange(cols) // FP8_BLOCK
         return s[:, ri][:, :, ci]
-    if fmt == FMT_FP8_TENSOR:
+    if fmt in (FMT_FP8_TENSOR, FMT_E5M2_TENSOR):
         s = np.asarray(scale, dtype=np.float32).astype(np.float64).reshape(batch, 1, 1)
         return np.broadcast_to(s, (batch, rows, cols))
     if fmt == FMT_MXFP4:
@@ -83,6 +86,8 @@ def code_values(fmt, data, batch, rows, cols):
         return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     if fmt in (FMT_FP8, FMT_FP8_TENSOR):
         return E4M3_TABLE[np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)]
+    if fmt == FMT_E5M2_TENSOR:
+        return E5M2_TABLE[np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)]
     if fmt in (FMT_MXFP4, FMT_NVFP4):
         packed = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols // 2)
         return E2M1_TABLE[unpack_fp4(packed, cols)]
@@ -95,7 +100,7 @@ def dequant_values(fmt, data, scale=None, tensor_scale=None, batch=1, rows=None,
     if fmt == FMT_BF16:
         return v
     s_bf = bf16_round(scale_values(fmt, scale, tensor_scale, batch, rows, cols))
-    v_bf = bf16_round(v)  # exact for every E4M3 and E2M1 value
+    v_bf = bf16_round(v)  # exact for every E4M3, E5M2 and E2M1 value
     return bf16_round(v_bf * s_bf)
 
 
@@ -120,11 +125,11 @@ def dequant_cols(fmt, data, scale, tensor_scale, rows, cols, col_idx, batch_idx=
         s = np.asarray(scale, dtype=np.float32).astype(np.float64)
         s = s.reshape(batch, -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK))[batch_idx]
         s = s[np.arange(rows) // FP8_BLOCK][:, col_idx // FP8_BLOCK]
-    elif fmt == FMT_FP8_TENSOR:
+    elif fmt in (FMT_FP8_TENSOR, FMT_E5M2_TENSOR):
         codes = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)[batch_idx][:, col_idx]
-        v = E4M3_TABLE[codes]
+        v = (E4M3_TABLE if fmt == FMT_FP8_TENSOR else E5M2_TABLE)[codes]
         s = float(np.asarray(scale, dtype=np.float32).reshape(batch)[batch_idx])
-    else:
+    elif fmt in (FMT_MXFP4, FMT_NVFP4):
         packed = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols // 2)[batch_idx]
         byte = packed[:, col_idx // 2]
         codes = np.where(col_idx % 2 == 0, byte & 0x0F, byte >> 4).astype(np.uint8)
@@ -136,6 +141,8 @@ def dequant_cols(fmt, data, scale, tensor_scale, rows, cols, col_idx, batch_idx=
             b = np.asarray(scale, dtype=np.uint8).reshape(batch, rows, cols // NV_BLOCK)[batch_idx]
             ts = float(np.asarray(tensor_scale, dtype=np.float32).reshape(batch)[batch_idx])
             s = fp32_round(E4M3_TABLE[b[:, col_idx // NV_BLOCK]] * ts)
+    else:
+        raise ValueError(f"unknown format {fmt!r}")
     return bf16_round(bf16_round(v) * bf16_round(s))
 
 
@@ -151,11 +158,11 @@ def dequant_rows(fmt, data, scale, tensor_scale, rows, cols, row_idx, batch_idx=
         s = np.asarray(scale, dtype=np.float32).astype(np.float64)
         s = s.reshape(batch, -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK))[batch_idx]
         s = s[row_idx // FP8_BLOCK][:, np.arange(cols) // FP8_BLOCK]
-    elif fmt == FMT_FP8_TENSOR:
+    elif fmt in (FMT_FP8_TENSOR, FMT_E5M2_TENSOR):
         codes = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols)[batch_idx][row_idx]
-        v = E4M3_TABLE[codes]
+        v = (E4M3_TABLE if fmt == FMT_FP8_TENSOR else E5M2_TABLE)[codes]
         s = float(np.asarray(scale, dtype=np.float32).reshape(batch)[batch_idx])
-    else:
+    elif fmt in (FMT_MXFP4, FMT_NVFP4):
         packed = np.asarray(data, dtype=np.uint8).reshape(batch, rows, cols // 2)[batch_idx][row_idx]
         v = E2M1_TABLE[unpack_fp4(packed, cols)]
         if fmt == FMT_MXFP4:
@@ -165,4 +172,6 @@ def dequant_rows(fmt, data, scale, tensor_scale, rows, cols, row_idx, batch_idx=
             b = np.asarray(scale, dtype=np.uint8).reshape(batch, rows, cols // NV_BLOCK)[batch_idx][row_idx]
             ts = float(np.asarray(tensor_scale, dtype=np.float32).reshape(batch)[batch_idx])
             s = fp32_round(E4M3_TABLE[b] * ts)[:, np.arange(cols) // NV_BLOCK]
+    else:
+        raise ValueError(f"unknown format {fmt!r}")
     return bf16_round(bf16_round(v) * bf16_round(s))

@@ -6,7 +6,9 @@ The pages name the formats but do not print their bit layouts:
   * E4M3 weights with float32 ``weight_scale_inv`` blocks -- transformers PR #50031,
     `_dequantize_fp8_weight`; E4M3 max 448 -- AstrAI fp8.py, FP8_MAX table;
   * E8M0 block scales (``float8_e8m0fnu``, group size 32) -- MindSpeed PR #3852,
-    `MXFP8MatMul.forward`.
+    `MXFP8MatMul.forward`;
+  * E5M2 for the gradient in the "hybrid" recipe (E4M3 forward, E5M2 backward), max
+    57344 -- AstrAI fp8.py, `FP8Format` and the FP8_MAX table.
 The layouts below are therefore taken from the public format definitions
 (OCP 8-bit Floating Point Specification; OCP Microscaling Formats v1.0) and
 written out code by code.
@@ -64,6 +66,52 @@ def _e8m0_value(b: int) -> float:
 
 
 E8M0_TABLE = np.array([_e8m0_value(b) for b in range(256)], dtype=np.float64)
+
+# --------------------------------------------------------------------------
+# E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent 0 is subnormal
+# (m/4 * 2^-14); exponent 31 is infinity (mantissa 0) or NaN (mantissa != 0).
+# --------------------------------------------------------------------------
+
+
+def _e5m2_value(code: int) -> float:
+    sign = -1.0 if (code >> 7) & 1 else 1.0
+    exp = (code >> 2) & 0x1F
+    man = code & 0x3
+    if exp == 0x1F:
+        return math.nan if man else sign * math.inf
+    if exp == 0:
+        return sign * (man / 4.0) * 2.0 ** -14
+    return sign * (1.0 + man / 4.0) * 2.0 ** (exp - 15)
+
+
+E5M2_TABLE = np.array([_e5m2_value(c) for c in range(256)], dtype=np.float64)
+E5M2_MAX = 57344.0  # AstrAI fp8.py FP8_MAX["e5m2"]
+
+
+def e5m2_round(x):
+    """E5M2 codes (uint8) of float64 values, rounded to the nearest E5M2 value, ties to
+    the even code (mantissa bit 0 clear).
+
+    Finite magnitudes beyond the largest finite value, and infinities, become +-57344
+    (saturation to the finite range); NaN becomes the code 0x7F (sign kept); the sign
+    of zero is kept.  The spacing of E5M2 values around |x| is 2^(floor(log2|x|) - 2)
+    for normal magnitudes and 2^-16 below 2^-14, so rint(x / spacing) * spacing is the
+    nearest-even value, as in bf16_round.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    finite = np.isfinite(ax) & (ax != 0)
+    r = np.zeros_like(ax)
+    _, e2 = np.frexp(ax[finite])
+    expo = np.maximum(e2 - 1, -14)
+    spacing = np.ldexp(1.0, expo - 2)
+    r[finite] = np.rint(ax[finite] / spacing) * spacing
+    r = np.where(np.isinf(ax) | (r > E5M2_MAX), E5M2_MAX, r)
+    # value -> code: the table's positive codes 0x00..0x7B hold every finite magnitude
+    # in increasing order
+    codes = np.searchsorted(E5M2_TABLE[:0x7C], r).astype(np.uint8)
+    codes = np.where(np.signbit(x), codes | 0x80, codes).astype(np.uint8)
+    return np.where(np.isnan(x), np.where(np.signbit(x), 0xFF, 0x7F), codes).astype(np.uint8)
 
 
 # --------------------------------------------------------------------------

@@ -88,3 +88,41 @@ def test_per_tensor_scale_of_the_wrong_expert_is_caught(monkeypatch):
 def test_untransposed_forward_is_caught(monkeypatch):
     monkeypatch.setattr(Gm, "forward", lambda x, w: Gm.as_f64(w) @ Gm.as_f64(x).T)
     assert _fails(TG.test_forward_brute_force, 3)
+
+
+def test_e5m2_rounding_half_up_is_caught(monkeypatch):
+    import tests.test_oracle_quantize as TQ
+    real_rint = np.rint
+
+    class HalfUp:                       # np.rint replaced by round-half-away inside e5m2_round
+        def __getattr__(self, name):
+            if name == "rint":
+                return lambda a: np.floor(np.asarray(a) + 0.5)
+            return getattr(np, name)
+    monkeypatch.setattr(F, "np", HalfUp())
+    assert _fails(TQ.test_e5m2_round_ties_to_even_at_every_midpoint)
+    assert real_rint is np.rint
+
+
+def test_e5m2_bias_error_is_caught(monkeypatch):
+    import tests.test_oracle_quantize as TQ
+    monkeypatch.setattr(F, "E5M2_TABLE", F.E5M2_TABLE * 2.0)
+    assert _fails(TQ.test_e5m2_table_matches_torch_float8)
+
+
+def test_amax_without_abs_is_caught(monkeypatch):
+    import oracle.quantize as Q
+    import tests.test_oracle_quantize as TQ
+
+    def signed_amax(g):
+        g = np.asarray(g, dtype=np.float64)
+        return float(max(F.fp32_round(np.max(g)), F.fp32_round(Q.AMAX_FLOOR)))
+    monkeypatch.setattr(Q, "amax_f32", signed_amax)
+    assert _fails(TQ.test_quantize_largest_element_lands_on_the_maximum)
+
+
+def test_step_from_the_e4m3_maximum_is_caught(monkeypatch):
+    import oracle.quantize as Q
+    import tests.test_oracle_quantize as TQ
+    monkeypatch.setattr(Q, "E5M2_MAX", F.E4M3_MAX)
+    assert _fails(TQ.test_quantize_matches_the_page_recipe_in_torch, 1.0)
