@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libbsq.so")
 HEADER_PATH = os.path.join(HERE, "..", "include", "bsq.h")
 
-BSQ_BF16, BSQ_FP8_E4M3_B128, BSQ_MXFP4, BSQ_NVFP4, BSQ_FP8_E4M3_TENSOR = 0, 1, 2, 3, 4
+BSQ_BF16, BSQ_FP8_E4M3_B128, BSQ_MXFP4, BSQ_NVFP4, BSQ_FP8_E4M3_TENSOR, BSQ_FP8_E5M2_TENSOR = 0, 1, 2, 3, 4, 5
 BSQ_OK, BSQ_ERR_INVALID_ARG, BSQ_ERR_UNSUPPORTED, BSQ_ERR_CUDA, BSQ_ERR_TIMEOUT = 0, 1, 2, 3, 4
 BSQ_NEEDS_GRAD_X, BSQ_NEEDS_GRAD_W = 1, 2
 
@@ -37,6 +37,10 @@ SIGNATURES = {
                            _i64, _c_void_p, _c_void_p],
     "bsq_linear_dgrad_smallm_noalloc": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i64,
                                         _c_void_p, _c_void_p],
+    "bsq_quantize_e5m2": [_c_void_p, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p],
+    "bsq_linear_backward_e5m2": [_c_void_p, _i64, _i64, _i32, _c_void_p, _c_void_p, _c_void_p, _i32, _c_void_p,
+                                 _c_void_p, _c_void_p, _i64, ctypes.c_uint32, _i32, _c_void_p, _c_void_p,
+                                 _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p],
     "bsq_status_string": [_i32],
     "bsq_last_error": [],
     "bsq_get_device_error": [ctypes.POINTER(_i32), _c_void_p],
@@ -167,6 +171,46 @@ def linear_backward(grad_out, w, x, needs=BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD_W, g
         _ptr(grad_x) if needs & BSQ_NEEDS_GRAD_X else None, _ptr(grad_w) if needs & BSQ_NEEDS_GRAD_W else None,
         _stream(stream)))
     return (grad_x if needs & BSQ_NEEDS_GRAD_X else None), (grad_w if needs & BSQ_NEEDS_GRAD_W else None)
+
+
+def quantize_e5m2(g, margin=0, codes=None, deq=None, want_deq=True, stream=None):
+    """Per-tensor E5M2 quantization of a BF16 gradient with its current amax:
+    (codes u8, step f32[1], amax f32[1], deq bf16 or None), all on g's device."""
+    dev = g.device
+    if codes is None:
+        codes = torch.empty(g.shape, dtype=torch.uint8, device=dev)
+    if deq is None and want_deq:
+        deq = torch.empty(g.shape, dtype=torch.bfloat16, device=dev)
+    step = torch.empty(1, dtype=torch.float32, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    _check(lib().bsq_quantize_e5m2(_ptr(g), g.numel(), margin, _ptr(codes), _ptr(deq), _ptr(step), _ptr(amax),
+                                   _stream(stream)))
+    return codes, step, amax, deq
+
+
+def linear_backward_e5m2(grad_out, w, x, needs=BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD_W, margin=0, grad_x=None,
+                         grad_w=None, stream=None):
+    """(grad_x, grad_w, step, amax): the backward on grad_out quantized once to E5M2 (step and
+    amax are the quantization's, f32[1] on the device)."""
+    M, N = grad_out.shape
+    K = (w if w is not None else x).cols
+    dev = grad_out.device
+    if needs & BSQ_NEEDS_GRAD_X and grad_x is None:
+        grad_x = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if needs & BSQ_NEEDS_GRAD_W and grad_w is None:
+        grad_w = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    codes = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    deq = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    step = torch.empty(1, dtype=torch.float32, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    f = lambda p, a: None if p is None else getattr(p, a)
+    _check(lib().bsq_linear_backward_e5m2(
+        _ptr(grad_out), M, N, f(w, "fmt") or 0, _ptr(f(w, "data")), _ptr(f(w, "scale")), _ptr(f(w, "tensor_scale")),
+        f(x, "fmt") or 0, _ptr(f(x, "data")), _ptr(f(x, "scale")), _ptr(f(x, "tensor_scale")), K, needs, margin,
+        _ptr(codes), _ptr(deq), _ptr(step), _ptr(amax),
+        _ptr(grad_x) if needs & BSQ_NEEDS_GRAD_X else None, _ptr(grad_w) if needs & BSQ_NEEDS_GRAD_W else None,
+        _stream(stream)))
+    return (grad_x if needs & BSQ_NEEDS_GRAD_X else None), (grad_w if needs & BSQ_NEEDS_GRAD_W else None), step, amax
 
 
 def linear_forward(x, w, out=None, stream=None):

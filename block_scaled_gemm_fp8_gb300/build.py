@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsq.so")
-SOURCES = ["bsq_api.cu", "bsq_dequant.cu", "bsq_gemm.cu", "bsq_smallm.cu", "bsq_forward.cu"]
+SOURCES = ["bsq_api.cu", "bsq_dequant.cu", "bsq_gemm.cu", "bsq_smallm.cu", "bsq_forward.cu", "bsq_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -65,7 +65,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Shared validation of a packed operand [batch][rows][cols].
 bsq_status check_packed(const char* what, int32_t fmt, const void* data, const void* scale, const float* ts,
                         int64_t batch, int64_t rows, int64_t cols, bool allow_bf16) {
-  if (fmt < BSQ_BF16 || fmt > BSQ_FP8_E4M3_TENSOR) return fail(BSQ_ERR_INVALID_ARG, "%s: unknown format %d", what, fmt);
+  if (fmt < BSQ_BF16 || fmt > BSQ_FP8_E5M2_TENSOR) return fail(BSQ_ERR_INVALID_ARG, "%s: unknown format %d", what, fmt);
   if (fmt == BSQ_BF16 && !allow_bf16) return fail(BSQ_ERR_UNSUPPORTED, "%s: BF16 is not a packed format here", what);
   if (batch < 0 || rows < 0 || cols < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
   const int64_t elems = batch * rows * cols;
@@ -75,7 +75,7 @@ bsq_status check_packed(const char* what, int32_t fmt, const void* data, const v
   if (fmt == BSQ_NVFP4 && elems > 0 && !ts) return fail(BSQ_ERR_INVALID_ARG, "%s: null tensor_scale", what);
   if (fmt == BSQ_FP8_E4M3_B128 && elems > 0 && !aligned16(scale))
     return fail(BSQ_ERR_INVALID_ARG, "%s: scale_inv not 16-byte aligned", what);
-  if (fmt == BSQ_FP8_E4M3_TENSOR && elems > 0 && (reinterpret_cast<uintptr_t>(scale) & 3u))
+  if ((fmt == BSQ_FP8_E4M3_TENSOR || fmt == BSQ_FP8_E5M2_TENSOR) && elems > 0 && (reinterpret_cast<uintptr_t>(scale) & 3u))
     return fail(BSQ_ERR_INVALID_ARG, "%s: scale_inv not 4-byte aligned", what);
   switch (fmt) {
     case BSQ_BF16:
@@ -83,6 +83,7 @@ bsq_status check_packed(const char* what, int32_t fmt, const void* data, const v
       break;
     case BSQ_FP8_E4M3_B128:
     case BSQ_FP8_E4M3_TENSOR:
+    case BSQ_FP8_E5M2_TENSOR:
       if (cols % 16) return fail(BSQ_ERR_UNSUPPORTED, "%s: FP8 cols %% 16 != 0 (row pitch must be 16 bytes)", what);
       break;
     case BSQ_MXFP4:
@@ -101,6 +102,8 @@ bsq_status check_packed(const char* what, int32_t fmt, const void* data, const v
 bsq_status check_gemm_common(const char* what, const void* g, int64_t S, int64_t N, int32_t fmt, int64_t K,
                              const void* out, int64_t out_elems) {
   if (S < 0 || N < 0 || K < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
+  if (fmt == BSQ_FP8_E5M2_TENSOR)
+    return fail(BSQ_ERR_UNSUPPORTED, "%s: E5M2 is the gradient's format (bsq_linear_backward_e5m2), not an operand's", what);
   if (S > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return fail(BSQ_ERR_UNSUPPORTED, "%s: size above 2^31-1", what);
   if (S * N > 0 && (!g || !aligned16(g))) return fail(BSQ_ERR_INVALID_ARG, "%s: grad_out null or not 16-byte aligned", what);
   if (N % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: N %% 8 != 0 (grad_out row pitch must be 16 bytes)", what);
@@ -208,7 +211,8 @@ bsq_status bsq_dequant(int32_t fmt, const void* data, const void* scale, const f
   if (st != BSQ_OK) return st;
   bsq::DequantArgs a{fmt, data, scale, tensor_scale, batch, rows, cols, out, sms, static_cast<cudaStream_t>(stream)};
   const char* msg = "";
-  if (bsq::launch_dequant(a, &msg) != 0) return fail(BSQ_ERR_CUDA, "bsq_dequant: %s", msg);
+  if ((fmt == BSQ_FP8_E5M2_TENSOR ? bsq::launch_dequant_e5m2(a, &msg) : bsq::launch_dequant(a, &msg)) != 0)
+    return fail(BSQ_ERR_CUDA, "bsq_dequant: %s", msg);
   return BSQ_OK;
 }
 
@@ -314,6 +318,8 @@ bsq_status bsq_linear_forward(int32_t x_fmt, const void* x_data, const void* x_s
   if (st != BSQ_OK) return st;
   st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, false);
   if (st != BSQ_OK) return st;
+  if (x_fmt == BSQ_FP8_E5M2_TENSOR || w_fmt == BSQ_FP8_E5M2_TENSOR)
+    return fail(BSQ_ERR_UNSUPPORTED, "%s: E5M2 is the gradient's format, not an operand's", what);
   if (bsq::kernel_fmt(x_fmt) != bsq::kernel_fmt(w_fmt))
     return fail(BSQ_ERR_UNSUPPORTED, "%s: X and W must share a packed format (FP8 blocks and per-tensor mix)", what);
   if (N % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: N %% 8 != 0 (Y row pitch must be 16 bytes)", what);
@@ -393,6 +399,54 @@ bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N, int32_t
   a.p_batch = 1; a.p_rows = S; a.kc = K; a.g = grad_out; a.S = S; a.N = N; a.offsets = offsets; a.E = E;
   a.out = grad_w; a.stream = static_cast<cudaStream_t>(stream);
   return run_gemm(a, what);
+}
+
+bsq_status bsq_quantize_e5m2(const void* g, int64_t n, int32_t margin, void* codes, void* deq, float* step,
+                             float* amax, void* stream) {
+  const char* what = "bsq_quantize_e5m2";
+  if (n < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
+  if (margin < 0 || margin > 30) return fail(BSQ_ERR_INVALID_ARG, "%s: margin %d outside 0..30", what, margin);
+  if (!step || !amax || (reinterpret_cast<uintptr_t>(step) & 3u) || (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return fail(BSQ_ERR_INVALID_ARG, "%s: step and amax must be 4-byte aligned device words", what);
+  if (n > 0 && (!g || !aligned16(g))) return fail(BSQ_ERR_INVALID_ARG, "%s: g null or not 16-byte aligned", what);
+  if (n > 0 && (!codes || (reinterpret_cast<uintptr_t>(codes) & 7u)))
+    return fail(BSQ_ERR_INVALID_ARG, "%s: codes null or not 8-byte aligned", what);
+  if (deq && !aligned16(deq)) return fail(BSQ_ERR_INVALID_ARG, "%s: deq not 16-byte aligned", what);
+  int32_t* err = nullptr;
+  int sms = 0;
+  bsq_status st = device_state(&err, &sms);
+  if (st != BSQ_OK) return st;
+  bsq::QuantArgs a{g, n, margin, codes, deq, step, amax, sms, static_cast<cudaStream_t>(stream)};
+  const char* msg = "";
+  if (bsq::launch_quantize_e5m2(a, &msg) != 0) return fail(BSQ_ERR_CUDA, "%s: %s", what, msg);
+  return BSQ_OK;
+}
+
+bsq_status bsq_linear_backward_e5m2(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
+                                    const void* w_scale, const float* w_tensor_scale, int32_t x_fmt,
+                                    const void* x_data, const void* x_scale, const float* x_tensor_scale, int64_t K,
+                                    uint32_t needs, int32_t margin, void* g_codes, void* g_deq, float* g_step,
+                                    float* g_amax, void* grad_x, void* grad_w, void* stream) {
+  const char* what = "bsq_linear_backward_e5m2";
+  if (needs & ~static_cast<uint32_t>(BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD_W))
+    return fail(BSQ_ERR_INVALID_ARG, "%s: unknown bits in needs (0x%x)", what, needs);
+  if (M < 0 || N < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
+  if (M * N > 0 && !g_deq) return fail(BSQ_ERR_INVALID_ARG, "%s: null g_deq", what);
+  // the products' own checks come first, so that a bad operand launches nothing
+  if (needs & BSQ_NEEDS_GRAD_X) {
+    const bsq_status st = static_cast<bsq_status>(
+        bsq::check_linear_dgrad_args(grad_out, M, N, w_fmt, w_data, w_scale, w_tensor_scale, K, grad_x));
+    if (st != BSQ_OK) return st;
+  }
+  if (needs & BSQ_NEEDS_GRAD_W) {
+    bsq_status st = check_gemm_common(what, grad_out, M, N, x_fmt, K, grad_w, N * K);
+    if (st == BSQ_OK) st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, true);
+    if (st != BSQ_OK) return st;
+  }
+  bsq_status st = bsq_quantize_e5m2(grad_out, M * N, margin, g_codes, g_deq, g_step, g_amax, stream);
+  if (st != BSQ_OK) return st;
+  return bsq_linear_backward(g_deq, M, N, w_fmt, w_data, w_scale, w_tensor_scale, x_fmt, x_data, x_scale,
+                             x_tensor_scale, K, needs, grad_x, grad_w, stream);
 }
 
 }  // extern "C"

@@ -67,6 +67,22 @@ struct DequantArgs {
 };
 
 int launch_dequant(const DequantArgs& a, const char** msg);
+// BSQ_FP8_E5M2_TENSOR codes with one float32 step per batch entry -> BF16 (bsq_quant.cu).
+int launch_dequant_e5m2(const DequantArgs& a, const char** msg);
+
+struct QuantArgs {
+  const void* g;      // bf16 [n]
+  int64_t n;
+  int margin;         // 0..30
+  void* codes;        // u8 [n] E5M2
+  void* deq;          // bf16 [n] or nullptr
+  float* step;        // f32 [1]
+  float* amax;        // f32 [1]; also the reduction word
+  int num_sms;
+  cudaStream_t stream;
+};
+// Per-tensor E5M2 quantization with the current amax (bsq_quant.cu).
+int launch_quantize_e5m2(const QuantArgs& a, const char** msg);
 
 struct SmallMArgs {
   int fmt;

@@ -32,8 +32,9 @@ FMT_FP8 = 1
 FMT_MXFP4 = 2
 FMT_NVFP4 = 3
 FMT_FP8_TENSOR = 4
+FMT_E5M2_TENSOR = 5
 FMT_NAMES = {FMT_BF16: "bf16", FMT_FP8: "fp8_e4m3_b128", FMT_MXFP4: "mxfp4", FMT_NVFP4: "nvfp4",
-             FMT_FP8_TENSOR: "fp8_e4m3_tensor"}
+             FMT_FP8_TENSOR: "fp8_e4m3_tensor", FMT_E5M2_TENSOR: "fp8_e5m2_tensor"}
 
 
 def _gen(device, seed):
@@ -196,10 +197,12 @@ def random_codes(fmt, batch, rows, cols, seed, device="cpu", scale_kind="random"
     replaced by 448 so that every decoded value is finite).
     """
     g = _gen(device, seed)
-    fp8 = fmt in (FMT_FP8, FMT_FP8_TENSOR)
+    fp8 = fmt in (FMT_FP8, FMT_FP8_TENSOR, FMT_E5M2_TENSOR)
     nbytes = cols if fp8 else cols // 2
     data = torch.randint(0, 256, (batch, rows, nbytes), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
-    if fp8 and scale_kind == "finite":
+    if fmt == FMT_E5M2_TENSOR and scale_kind == "finite":
+        data = torch.where((data & 0x7C) == 0x7C, data - 4, data)   # S.11111.mm (inf, NaN) -> S.11110.mm
+    elif fp8 and scale_kind == "finite":
         data = torch.where((data & 0x7F) == 0x7F, data - 1, data)   # S.1111.111 (NaN) -> S.1111.110 (448)
     ts = None
     if fp8:
@@ -208,7 +211,8 @@ def random_codes(fmt, batch, rows, cols, seed, device="cpu", scale_kind="random"
         if scale_kind == "finite":
             # |code| <= 448 and scale < 2^117 keep every product below the BF16 maximum
             mant = torch.rand(shape, generator=g, device=device) + 1.0
-            exps = torch.tensor([-137, -134, -131, -128, -125, -121, -60, -7, -3, 0, 5, 40, 100, 116],
+            exps = torch.tensor([-137, -134, -131, -128, -125, -121, -60, -7, -3, 0, 5, 40, 100,
+                                 100 if fmt == FMT_E5M2_TENSOR else 116],   # E5M2 codes reach 2^15.8
                                 dtype=torch.float32, device=device)
             ex = exps[torch.randint(0, exps.numel(), shape, generator=g, device=device)]
             s = mant * torch.pow(2.0, ex)

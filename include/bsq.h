@@ -33,6 +33,9 @@
  *       BSQ_FP8_E4M3_TENSOR data u8 [batch][rows][cols]; scale f32[batch] (one scale_inv per
  *                          tensor -- per expert for a grouped weight -- broadcast over it:
  *                          transformers PR #50031 `_dequantize_fp8_weight`, block_size None)
+ *       BSQ_FP8_E5M2_TENSOR data u8 [batch][rows][cols] E5M2 codes; scale f32[batch] (one
+ *                          quantization step per tensor, bsq_quantize_e5m2); dequantized by
+ *                          the same rule with the step as the scale
  *       BSQ_MXFP4          data u8  [batch][rows][cols/2]; scale u8 [batch][rows][cols/32]
  *       BSQ_NVFP4          data u8  [batch][rows][cols/2]; scale u8 (E4M3) [batch][rows][cols/16];
  *                          tensor_scale f32[batch]
@@ -97,7 +100,8 @@ typedef enum {
   BSQ_FP8_E4M3_B128 = 1,
   BSQ_MXFP4 = 2,
   BSQ_NVFP4 = 3,
-  BSQ_FP8_E4M3_TENSOR = 4
+  BSQ_FP8_E4M3_TENSOR = 4,
+  BSQ_FP8_E5M2_TENSOR = 5   /* the quantized gradient: bsq_dequant only, not a GEMM operand */
 } bsq_format;
 
 /* Device error word values (bsq_get_device_error). */
@@ -226,6 +230,35 @@ bsq_status bsq_linear_dgrad_smallm_noalloc(const void* grad_out, int64_t M, int6
                                            int32_t w_fmt, const void* w_data, const void* w_scale,
                                            const float* w_tensor_scale, int64_t K, void* grad_x,
                                            void* stream);
+
+/*
+ * bsq_quantize_e5m2 -- per-tensor E5M2 quantization of a BF16 gradient with the current
+ * amax (AstrAI fp8.py, `_LinearFp8.backward` in the "hybrid" format and `_dynamic_scale`):
+ *   amax = max |g| (float32, at least 1e-12; NaN when g holds a NaN),
+ *   step = (amax / 57344) / 2^margin   (float32 divisions),
+ *   codes[i] = E5M2 of g[i] / step     (float32 division, nearest even, saturating to +-57344).
+ * g: bf16[n], 16-byte aligned.  codes: u8[n], 8-byte aligned.  deq (optional, may be NULL):
+ * bf16[n], 16-byte aligned, receives bf16(bf16(code) * bf16(step)) -- what bsq_dequant of
+ * the codes gives.  step, amax: one f32 each (device); amax also serves as the kernels'
+ * reduction word, so it must not alias step or the inputs.  0 <= margin <= 30.
+ */
+bsq_status bsq_quantize_e5m2(const void* g, int64_t n, int32_t margin, void* codes, void* deq, float* step,
+                             float* amax, void* stream);
+
+/*
+ * bsq_linear_backward_e5m2 -- the backward with a quantized gradient: grad_out is quantized
+ * once to E5M2 (bsq_quantize_e5m2 into g_codes, g_deq, g_step, g_amax) and both products
+ * of bsq_linear_backward run on the dequantized copy g_deq (AstrAI fp8.py,
+ * `_LinearFp8.backward`: one quantization shared by dX and dW, masks from
+ * needs_input_grad, the gradient's amax returned for the caller's history).
+ * g_codes u8[M][N] and g_deq bf16[M][N] are caller-owned scratch; the other arguments are
+ * those of bsq_linear_backward.  Every operand check runs before anything is launched.
+ */
+bsq_status bsq_linear_backward_e5m2(const void* grad_out, int64_t M, int64_t N, int32_t w_fmt, const void* w_data,
+                                    const void* w_scale, const float* w_tensor_scale, int32_t x_fmt,
+                                    const void* x_data, const void* x_scale, const float* x_tensor_scale, int64_t K,
+                                    uint32_t needs, int32_t margin, void* g_codes, void* g_deq, float* g_step,
+                                    float* g_amax, void* grad_x, void* grad_w, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* bsq_status_string(int32_t status);

@@ -10,7 +10,8 @@ from oracle import formats as F
 from oracle import gemm as Gm
 
 ORACLE_FMT = {synth.FMT_BF16: D.FMT_BF16, synth.FMT_FP8: D.FMT_FP8, synth.FMT_MXFP4: D.FMT_MXFP4,
-              synth.FMT_NVFP4: D.FMT_NVFP4, synth.FMT_FP8_TENSOR: D.FMT_FP8_TENSOR}
+              synth.FMT_NVFP4: D.FMT_NVFP4, synth.FMT_FP8_TENSOR: D.FMT_FP8_TENSOR,
+              synth.FMT_E5M2_TENSOR: D.FMT_E5M2_TENSOR}
 
 
 def oracle_deq(p):

@@ -86,7 +86,8 @@ def test_linear_backward_validation(L):
 def test_fp8_per_tensor_format_validation(L):
     assert _dgrad(L, fmt=4, K=40) == bsq.BSQ_ERR_UNSUPPORTED            # FP8 row pitch: K % 16
     assert _dgrad(L, fmt=4, s=FAKE + 2) == bsq.BSQ_ERR_INVALID_ARG       # scale_inv must be 4-byte aligned
-    assert _dgrad(L, fmt=5) == bsq.BSQ_ERR_INVALID_ARG                   # no such format
+    assert _dgrad(L, fmt=6) == bsq.BSQ_ERR_INVALID_ARG                   # no such format
+    assert _dgrad(L, fmt=5) == bsq.BSQ_ERR_UNSUPPORTED                   # E5M2: the gradient's format only
     assert L.bsq_dequant(4, FAKE, FAKE + 4, None, 0, 4, 32, FAKE, None) == bsq.BSQ_OK
     # the allocation-free small-M entry point serves 128 x 128 FP8 blocks only
     assert L.bsq_linear_dgrad_smallm_noalloc(FAKE, 4, 64, 4, FAKE, FAKE, None, 256, FAKE, None) == \
@@ -101,3 +102,30 @@ def test_linear_forward_validation(L):
     assert fw(N=12) == bsq.BSQ_ERR_UNSUPPORTED          # Y row pitch
     assert fw(y=None) == bsq.BSQ_ERR_INVALID_ARG
     assert fw(M=0) == bsq.BSQ_OK and fw(N=0) == bsq.BSQ_OK
+
+
+def test_e5m2_gradient_validation(L):
+    def q(g=FAKE, n=64, margin=0, codes=FAKE, deq=None, step=FAKE + 64, amax=FAKE + 128):
+        return L.bsq_quantize_e5m2(g, n, margin, codes, deq, step, amax, None)
+    assert q(margin=-1) == bsq.BSQ_ERR_INVALID_ARG and q(margin=31) == bsq.BSQ_ERR_INVALID_ARG
+    assert q(n=-1) == bsq.BSQ_ERR_INVALID_ARG
+    assert q(g=FAKE + 8) == bsq.BSQ_ERR_INVALID_ARG          # g must be 16-byte aligned
+    assert q(codes=FAKE + 4) == bsq.BSQ_ERR_INVALID_ARG      # codes 8-byte aligned
+    assert q(deq=FAKE + 8) == bsq.BSQ_ERR_INVALID_ARG        # deq 16-byte aligned
+    assert q(step=None) == bsq.BSQ_ERR_INVALID_ARG and q(amax=FAKE + 2) == bsq.BSQ_ERR_INVALID_ARG
+    # E5M2 is no GEMM operand and no forward operand
+    assert L.bsq_linear_wgrad(FAKE, 64, 64, 5, FAKE, FAKE, None, 64, FAKE, None) == bsq.BSQ_ERR_UNSUPPORTED
+    assert L.bsq_linear_forward(5, FAKE, FAKE, None, 64, 5, FAKE, FAKE, None, 64, 64, FAKE, None) == \
+        bsq.BSQ_ERR_UNSUPPORTED
+    # the E5M2 backward checks its products' operands before anything runs
+    def bw(wf=2, xf=2, needs=3, deq=FAKE, N=64):
+        return L.bsq_linear_backward_e5m2(FAKE, 64, N, wf, FAKE, FAKE, None, xf, FAKE, FAKE, None, 64, needs, 0,
+                                          FAKE, deq, FAKE + 64, FAKE + 128, FAKE, FAKE, None)
+    assert bw(needs=4) == bsq.BSQ_ERR_INVALID_ARG
+    assert bw(deq=None) == bsq.BSQ_ERR_INVALID_ARG
+    assert bw(wf=5) == bsq.BSQ_ERR_UNSUPPORTED and bw(xf=5, needs=2) == bsq.BSQ_ERR_UNSUPPORTED
+    assert bw(N=12) == bsq.BSQ_ERR_UNSUPPORTED                # grad_out row pitch
+    # dequantizing E5M2 codes: a per-tensor step, FP8 row pitch
+    assert L.bsq_dequant(5, FAKE, FAKE + 4, None, 1, 4, 40, FAKE, None) == bsq.BSQ_ERR_UNSUPPORTED
+    assert L.bsq_dequant(5, FAKE, FAKE + 2, None, 1, 4, 32, FAKE, None) == bsq.BSQ_ERR_INVALID_ARG
+    assert L.bsq_dequant(5, FAKE, FAKE + 4, None, 0, 4, 32, FAKE, None) == bsq.BSQ_OK

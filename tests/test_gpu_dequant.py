@@ -9,7 +9,7 @@ from tests._util import oracle_deq_bits, same_bits
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4, synth.FMT_FP8_TENSOR]
+FMTS = [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4, synth.FMT_FP8_TENSOR, synth.FMT_E5M2_TENSOR]
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -25,7 +25,7 @@ def test_dequant_bit_exact(fmt, kind, shape):
     assert same_bits(got, ref), f"mismatches: {(got != ref).sum()}"
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", FMTS[:4])   # E5M2 codes come from bsq_quantize_e5m2 (test_gpu_e5m2.py)
 def test_dequant_quantized_values(fmt):
     p = synth.make_packed(fmt, 2, 256, 512, 1.0, seed=3, device="cpu")
     ref = oracle_deq_bits(p).reshape(2, 256, 512)
