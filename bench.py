@@ -51,7 +51,7 @@ def parse_args():
                     help="time only the headline workload (not the other four, nor the standalone dequant)")
     ap.add_argument("--profile", default=None,
                     choices=["backward", "dgrad", "wgrad", "grouped_dgrad", "grouped_wgrad", "small_m", "dequant",
-                             "forward"],
+                             "forward", "e5m2"],
                     help="run only this op of the workload, --warmup + --steps times back to back, and print "
                          "its mean time (a fixed launch sequence for ncu; not a benchmark line)")
     ap.add_argument("--experts", type=int, default=None,
@@ -83,6 +83,10 @@ def profile_run(args, bsq, synth, dev):
     elif op == "forward":
         yo = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
         f = lambda: bsq.linear_forward(c["X"], c["W"], out=yo)
+    elif op == "e5m2":
+        qc = torch.empty(c["G"].shape, dtype=torch.uint8, device=dev)
+        qd = torch.empty(c["G"].shape, dtype=torch.bfloat16, device=dev)
+        f = lambda: bsq.quantize_e5m2(c["G"], codes=qc, deq=qd)
     elif op == "small_m":
         if "G_small" not in c:
             c["G_small"] = synth.randn((16, c["N"]), 1e-2, 7, dev, torch.bfloat16)
@@ -181,7 +185,7 @@ def op_roofline(flops, nbytes, ms, pk):
 
 # The GEMM kernel's sources: a traffic figure captured from an earlier build is reported
 # only while these are unchanged.
-KERNEL_SOURCES = ["bsq_gemm.cu", "bsq_decode.cuh", "bsq_ptx.cuh", "bsq_internal.h"]
+KERNEL_SOURCES = ["bsq_gemm.cu", "bsq_decode.cuh", "bsq_ptx.cuh", "bsq_pipe.cuh", "bsq_internal.h"]
 
 
 def kernel_source_sha1():
@@ -498,6 +502,8 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
         ms, nbytes = time_small_m(c, bsq, steps, warmup, flush)
         r["small_m_dgrad"] = {"M": 16, "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
                               "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": nbytes}
+    if n == 4:
+        r["grouped_decode_dgrad"] = measure_grouped_decode(c, bsq, synth, steps, warmup, flush, pk)
     deq = None
     if n in DEQUANT_WORKLOADS:
         deq = measure_dequant(c["W"], bsq, steps, warmup, flush, pk)
@@ -536,6 +542,62 @@ def measure_forward(c, bsq, steps, warmup, flush, pk):
 # the M = 16 dgrad on the headline weight and on these.
 DEQUANT_WORKLOADS = (3, 4, 5)
 SMALL_M_WORKLOADS = (3,)
+DECODE_ROWS = 64   # a decode-sized grouped batch: routed rows over the grouped workload's experts
+
+
+def _timed(f, steps, warmup, flush):
+    """Median ms of f() with L2 flushed before each timed call (CUDA events, current stream)."""
+    for _ in range(warmup):
+        f()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        f()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def measure_grouped_decode(c, bsq, synth, steps, warmup, flush, pk, rows=DECODE_ROWS):
+    """Grouped dgrad of a decode-sized batch (`rows` grad_out rows routed over the workload's
+    experts by the same law) through bsq_grouped_dgrad: GB/s of algorithmic bytes -- the
+    packed weights and scales of the experts that received rows, read once, plus grad_out
+    and grad_x."""
+    E, N, K, W = c["E"], c["N"], c["K"], c["W"]
+    counts = synth.zipf_counts(rows, E, 1.1, 5, force_empty=[e for e in (0, 31, 63) if e < E])
+    offs = torch.from_numpy(synth.offsets_from_counts(counts)).to(c["G"].device)
+    G = synth.randn((rows, N), 1.0, 3, c["G"].device, torch.bfloat16)
+    out = torch.empty((rows, K), dtype=torch.bfloat16, device=G.device)
+    ms = _timed(lambda: bsq.grouped_dgrad(G, W, offs, out=out), steps, warmup, flush)
+    active = int((counts > 0).sum())
+    nbytes = packed_bytes(W) * active / E + 2.0 * rows * N + 2.0 * rows * K
+    return {"rows": rows, "experts_routed": active, "ms": ms, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "kernel": "smallm_dgrad_cluster_kernel"}
+
+
+def measure_e5m2(c, outs, bsq, steps, warmup, flush, pk):
+    """The quantized-gradient backward on the workload: bsq_linear_backward_e5m2 whole (the
+    gradient's E5M2 quantization, then both products), and bsq_quantize_e5m2 alone (GB/s of
+    2 bytes read, 1 byte of codes and 2 of the dequantized copy written per element)."""
+    G, M, N, K = c["G"], c["M"], c["N"], c["K"]
+    codes = torch.empty((M, N), dtype=torch.uint8, device=G.device)
+    deq = torch.empty((M, N), dtype=torch.bfloat16, device=G.device)
+    q_ms = _timed(lambda: bsq.quantize_e5m2(G, codes=codes, deq=deq), steps, warmup, flush)
+    b_ms = _timed(lambda: bsq.linear_backward_e5m2(G, c["W"], c["X"], grad_x=outs["dgrad"], grad_w=outs["wgrad"]),
+                  steps, warmup, flush)
+    qb = 5.0 * M * N
+    fl = 4.0 * M * N * K
+    return {"backward_ms": b_ms, "backward_tflops": fl / (b_ms * 1e-3) / 1e12,
+            "quantize": {"ms": q_ms, "algorithmic_bytes": qb, "GB/s": qb / (q_ms * 1e-3) / 1e9,
+                         "frac_hbm": qb / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                         "kernels": "amax_bf16_kernel + quantize_e5m2_kernel"}}
 
 
 def measure_dequant(p, bsq, steps, warmup, flush, pk):
@@ -745,6 +807,8 @@ def main():
         line["small_m_dgrad"] = {"M": int(c["G_small"].shape[0]), "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
                                  "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                  "algorithmic_bytes": nbytes}
+    if args.config == 2:
+        line["e5m2_backward"] = measure_e5m2(c, outs, bsq, max(5, args.steps // 2), args.warmup, flush, pk)
     if not args.no_e2e:
         ms, h2d, d2h = time_e2e(c, outs, bsq, max(3, args.steps // 2), 2)
         line["e2e"] = {"value": world * flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
