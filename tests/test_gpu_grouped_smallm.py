@@ -138,7 +138,7 @@ def test_grouped_workload_weights_decode_batch(rows):
     assert st == bsq.BSQ_OK and code == 0
 
 
-def test_bad_offsets_reported_nothing_written():
+def test_bad_offsets_reported_nothing_written(monkeypatch):
     N, K, S = 128, 256, 40
     W = synth.make_packed(synth.FMT_MXFP4, 3, N, K, 1.0, seed=80, device="cpu").to("cuda")
     G = synth.randn((S, N), 1.0, 81, "cpu", torch.bfloat16).cuda()
@@ -153,7 +153,9 @@ def test_bad_offsets_reported_nothing_written():
     assert (out.float() == 7.0).all()
     st, code = bsq.get_device_error()
     assert st == bsq.BSQ_OK and code == 0
-    # S above the bound: the GEMM and the small-M kernel both run, both see the bad offsets
+    # S above the bound with a tail bound set: the GEMM and the small-M kernel both run,
+    # both see the bad offsets
+    monkeypatch.setenv("BSQ_GROUPED_TAIL_ROWS", "64")
     S2 = 300
     G2 = synth.randn((S2, N), 1.0, 82, "cpu", torch.bfloat16).cuda()
     out2 = torch.full((S2, K), 7.0, dtype=torch.bfloat16, device="cuda")
