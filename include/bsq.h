@@ -221,7 +221,9 @@ bsq_status bsq_grouped_wgrad(const void* grad_out, int64_t S, int64_t N,
  * BSQ_ERR_UNSUPPORTED (or the usual argument errors) without launching.
  * Allocation: calls no cudaMalloc / cudaFree or any allocating routine.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.
+ * current, and the address is kept for the life of the process; make that first call
+ * before any stream capture.  A cudaDeviceReset invalidates the kept address: this entry
+ * point is not to be called on a device after it was reset.
  * Sharing: every call uses the same array and clears the part it needs on `stream` before
  * its kernel; calls whose work overlaps on the GPU (different streams) race on the array
  * and must be ordered by the caller.
