@@ -311,16 +311,13 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       const int nchunks = (n_valid + 15) >> 4;
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kNTile;
       __nv_bfloat16* yrow = p.y + static_cast<int64_t>(m) * p.N + n0;
-      uint32_t v[16];
-      tmem_ld_32x32b_x16(trow, v);
       for (int c = 0; c < nchunks; ++c) {
-        tmem_wait_ld();
+        uint32_t v[16];
+        tmem_ld_32x32b_x16_wait(trow + c * 16, v);   // the load completes inside the statement
         uint32_t h[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-        if (c + 1 < nchunks) {
-          tmem_ld_32x32b_x16(trow + (c + 1) * 16, v);
-        } else {
+        if (c + 1 == nchunks) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {

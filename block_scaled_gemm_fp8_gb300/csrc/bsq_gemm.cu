@@ -652,19 +652,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_acc();   // no chunk for this warp: release at once
         continue;
       }
-      // The chunks of this warp, pipelined: once a chunk's TMEM load has landed it is packed
-      // to BF16 pairs, the next chunk's load is issued, and the packed chunk is stored while
-      // that load is in flight.
+      // The chunks of this warp: each TMEM load completes inside its own statement (see
+      // tmem_ld_32x32b_x16_wait); the accumulator is released after the warp's last load.
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN;
-      uint32_t v[16];
-      tmem_ld_32x32b_x16(trow + sub * 16, v);
       for (int c = sub; c < nchunks; c += R::kEpiPerQuarter) {
-        tmem_wait_ld();
+        uint32_t v[16];
+        tmem_ld_32x32b_x16_wait(trow + c * 16, v);
+        if (c + R::kEpiPerQuarter >= nchunks) release_acc();   // every TMEM read of this warp has completed
         uint32_t h[8];   // (n, n+1) pairs of this thread's column m, BF16
 #pragma unroll
         for (int j = 0; j < 8; ++j) h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-        if (c + R::kEpiPerQuarter < nchunks) tmem_ld_32x32b_x16(trow + (c + R::kEpiPerQuarter) * 16, v);
-        else release_acc();   // every TMEM read of this warp has completed
         if (mok) {
           const int nlim = min(16, ti.n_valid - c * 16);
           const int64_t step = p.Kc;
