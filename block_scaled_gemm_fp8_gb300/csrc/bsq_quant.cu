@@ -8,10 +8,21 @@
 // the finite range.  A dequantized copy, bf16(bf16(code) * bf16(step)) -- the library's
 // dequantization rule -- can be written in the same pass.
 //
-// Two passes over the gradient, both bound by HBM: an amax reduction (16-byte loads, one
-// atomic max per block on the float's bits, which order like the values for non-negative
-// floats and put NaN above infinity), then the quantization (16-byte loads, 8-byte code
-// stores, 16-byte stores of the dequantized copy).
+// Two passes over the gradient, both bound by HBM: an amax reduction (four independent
+// 16-byte loads in flight per thread, one atomic max per block on the float's bits, which
+// order like the values for non-negative floats and put NaN above infinity), then the
+// quantization (16-byte loads, 8-byte code stores, 16-byte stores of the dequantized copy).
+//
+// The quotient.  The code of an element is RN_e5m2(RN_f32(x / step)).  The quantization
+// pass forms q1 = RN_f32(x * r) with r = RN_f32(1 / step) instead of dividing: q1 is within
+// 3 float32 ulps of the IEEE quotient (two roundings of relative size 2^-24 each, the
+// quotient's own half ulp, and up to a factor 2 from the position in the binade).  E5M2
+// rounding is monotonic and changes only at the midpoints between neighbouring E5M2
+// values, which in float32 are the numbers whose 23-bit mantissa has bit 20 set and bits
+// 19..0 clear.  So when q1's low 21 mantissa bits are more than 4 away from that pattern,
+// q1 and the quotient round to the same code; otherwise, and below 2^-13 (the E5M2
+// subnormal range and its edge), the element takes the IEEE division.  Zeros, infinities
+// and NaNs give the same codes either way (r is 0 when step is infinite, NaN when it is).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -33,15 +44,21 @@ __device__ __forceinline__ uint32_t abs_max_pair(uint32_t w) {
   return a > b ? a : b;
 }
 
+__device__ __forceinline__ uint32_t abs_max_u4(const uint4& v) {
+  return max(max(abs_max_pair(v.x), abs_max_pair(v.y)), max(abs_max_pair(v.z), abs_max_pair(v.w)));
+}
+
 __global__ void __launch_bounds__(kQThreads) amax_bf16_kernel(const uint4* __restrict__ g, int64_t n8,
                                                                const uint16_t* __restrict__ tail, int tail_n,
                                                                uint32_t* __restrict__ amax_bits) {
   uint32_t m = 0;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * kQThreads) {
-    const uint4 v = __ldg(g + i);
-    m = max(m, max(max(abs_max_pair(v.x), abs_max_pair(v.y)), max(abs_max_pair(v.z), abs_max_pair(v.w))));
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kQThreads;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {   // four loads in flight
+    const uint4 a = __ldg(g + i), b = __ldg(g + i + stride), c = __ldg(g + i + 2 * stride), d = __ldg(g + i + 3 * stride);
+    m = max(m, max(max(abs_max_u4(a), abs_max_u4(b)), max(abs_max_u4(c), abs_max_u4(d))));
   }
+  for (; i < n8; i += stride) m = max(m, abs_max_u4(__ldg(g + i)));
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail_n) m = max(m, static_cast<uint32_t>(tail[threadIdx.x] & 0x7FFFu));
   m = __reduce_max_sync(0xffffffffu, m);
   __shared__ uint32_t wm[kQThreads / 32];
@@ -78,6 +95,17 @@ __device__ __forceinline__ uint32_t e5m2x2_dequant(uint32_t c, float s) {
 
 __device__ __forceinline__ float bf16_round_f(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
+// RN_f32(x / step), from q1 = x * rcp where that gives the same E5M2 code (see the top of
+// the file), else from the IEEE division.
+__device__ __forceinline__ float e5m2_quotient(float x, float step, float rcp) {
+  const float q = x * rcp;
+  const uint32_t u = __float_as_uint(q) & 0x7FFFFFFFu;
+  const uint32_t low = u & 0x1FFFFFu;
+  const bool near_mid = low - 0xFFFFCu <= 8u;         // |low - 0x100000| <= 4
+  const bool small = u < 0x39000000u && u != 0u;      // 0 < |q1| < 2^-13
+  return (near_mid || small) ? __fdiv_rn(x, step) : q;
+}
+
 __global__ void __launch_bounds__(kQThreads) quantize_e5m2_kernel(const uint4* __restrict__ g, int64_t n8,
                                                                    const uint16_t* __restrict__ g_tail, int tail_n,
                                                                    uint32_t* __restrict__ amax_bits, int margin,
@@ -86,20 +114,31 @@ __global__ void __launch_bounds__(kQThreads) quantize_e5m2_kernel(const uint4* _
                                                                    float* __restrict__ step_out) {
   const float amax = amax_of(*reinterpret_cast<volatile uint32_t*>(amax_bits));
   const float step = __fdiv_rn(__fdiv_rn(amax, kE5M2Max), __int_as_float((127 + margin) << 23));   // margin 0..30
+  const float rcp = __frcp_rn(step);
   const float s_bf = bf16_round_f(step);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * kQThreads) {
-    const uint4 v = __ldg(g + i);
+  // eight elements at index i: codes, and the dequantized copy when asked for
+  auto put = [&](const uint4& v, int64_t i) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t c2[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      c2[j] = e5m2x2(__fdiv_rn(__uint_as_float(w[j] << 16), step), __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), step));
+      c2[j] = e5m2x2(e5m2_quotient(__uint_as_float(w[j] << 16), step, rcp),
+                     e5m2_quotient(__uint_as_float(w[j] & 0xFFFF0000u), step, rcp));
     codes[i] = make_uint2(c2[0] | (c2[1] << 16), c2[2] | (c2[3] << 16));
     if (deq)
       deq[i] = make_uint4(e5m2x2_dequant(c2[0], s_bf), e5m2x2_dequant(c2[1], s_bf), e5m2x2_dequant(c2[2], s_bf),
                           e5m2x2_dequant(c2[3], s_bf));
+  };
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kQThreads;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {   // four loads in flight
+    const uint4 a = __ldg(g + i), b = __ldg(g + i + stride), c = __ldg(g + i + 2 * stride), d = __ldg(g + i + 3 * stride);
+    put(a, i);
+    put(b, i + stride);
+    put(c, i + 2 * stride);
+    put(d, i + 3 * stride);
   }
+  for (; i < n8; i += stride) put(__ldg(g + i), i);
   if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail_n) {
     const float x = __uint_as_float(static_cast<uint32_t>(g_tail[threadIdx.x]) << 16);
     const uint32_t c = e5m2x2(__fdiv_rn(x, step), 0.f) & 0xFFu;
@@ -132,8 +171,9 @@ __global__ void __launch_bounds__(kQThreads) dequant_e5m2_kernel(const uint2* __
 int launch_quantize_e5m2(const QuantArgs& a, const char** msg) {
   const int64_t n8 = a.n / 8;
   const int tail = static_cast<int>(a.n % 8);
-  int64_t blocks = (n8 + kQThreads - 1) / kQThreads;
-  const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
+  // four resident blocks of 256 threads per SM, each thread with four 16-byte loads in flight
+  int64_t blocks = (n8 + 4 * kQThreads - 1) / (4 * kQThreads);
+  const int64_t cap = static_cast<int64_t>(a.num_sms) * 4;
   blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
   const uint16_t* g16 = static_cast<const uint16_t*>(a.g);
   uint8_t* c8 = static_cast<uint8_t*>(a.codes);

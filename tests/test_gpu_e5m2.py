@@ -76,6 +76,20 @@ def test_quantize_every_bf16_pattern():
     _check_quantize(finite.clone())
 
 
+def test_quantize_bit_exact_across_steps():
+    """Every finite BF16 value of magnitude up to amax, for 48 amax values from 2^-30 to
+    2^30 and margins 0..3: the kernel divides through the reciprocal of the step and takes
+    the IEEE division where the product lies within a few ulps of an E5M2 rounding
+    midpoint or below 2^-13; every element must still match the float32 quotient's code."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    finite = bits[torch.isfinite(bits.float())]
+    rng = np.random.default_rng(17)
+    for a in rng.uniform(-30.0, 30.0, 48):
+        amax = torch.tensor([2.0 ** a * rng.uniform(1.0, 2.0)]).to(torch.bfloat16)
+        g = torch.cat([finite[finite.float().abs() <= amax.float()], amax, -amax])
+        _check_quantize(g.clone(), margin=int(rng.integers(0, 4)))
+
+
 @pytest.mark.parametrize("fmt", [synth.FMT_MXFP4, synth.FMT_FP8])
 @pytest.mark.parametrize("M,N,K", [(300, 256, 384), (8, 512, 256), (1024, 1024, 1024)])
 @pytest.mark.parametrize("needs", [3, 1, 2])
