@@ -227,8 +227,11 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
 // written when the statement ends, and may copy, move or spill them from then on.  A load
 // and its tcgen05.wait::ld in separate statements therefore leave a window in which the
 // compiler can read the registers before the hardware has filled them; one statement
-// closes it.
+// closes it.  Both instructions are .sync.aligned: every lane of the warp must execute
+// them together, so the warp is reconverged first (callers reach them after lane-dependent
+// branches, and nothing else guarantees reconvergence there).
 __device__ __forceinline__ void tmem_ld_32x32b_x16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+  __syncwarp();
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
