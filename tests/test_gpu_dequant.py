@@ -25,6 +25,19 @@ def test_dequant_bit_exact(fmt, kind, shape):
     assert same_bits(got, ref), f"mismatches: {(got != ref).sum()}"
 
 
+@pytest.mark.parametrize("kind", ["random", "edge", "nan"])
+@pytest.mark.parametrize("shape", [(2, 3, 48), (1, 5, 16), (3, 7, 80)])
+def test_dequant_nvfp4_half_groups(kind, shape):
+    """NVFP4 operands whose batch entries hold an odd number of 16-code scale groups (the
+    last 4-byte word of a batch entry and the first of the next share a warp load)."""
+    B, R, C = shape
+    p = synth.random_codes(synth.FMT_NVFP4, B, R, C, seed=7 * B + R + C, scale_kind=kind)
+    ref = oracle_deq_bits(p).reshape(B, R, C)
+    out = bsq.dequant(p.to("cuda"))
+    torch.cuda.synchronize()
+    assert same_bits(synth.bf16_numpy(out).reshape(B, R, C), ref)
+
+
 @pytest.mark.parametrize("fmt", FMTS[:4])   # E5M2 codes come from bsq_quantize_e5m2 (test_gpu_e5m2.py)
 def test_dequant_quantized_values(fmt):
     p = synth.make_packed(fmt, 2, 256, 512, 1.0, seed=3, device="cpu")
