@@ -388,6 +388,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           wa = lds128(pst + F::kTileBytes + p_off);
           if (!F::kFp4) wb = lds128(pst + F::kTileBytes + p_off + 16);
         }
+        // this lane's plain loads from the slot are performed before its TMA refill (see the
+        // same release in bsq_gemm.cu)
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));
         uint32_t v[4][4];

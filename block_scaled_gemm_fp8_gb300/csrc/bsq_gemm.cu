@@ -108,7 +108,7 @@ static_assert(kUStages >= 2, "the MMA issuer awaits the next unit before committ
 static_assert(kDeqTeams == kUnitKb, "dequant team t fills k-block t of every unit");
 constexpr int kMaxStages = 8;
 
-template <int FMT>
+template <int FMT, bool SHORT = false>
 struct Fmt {
   static constexpr bool kFp4 = FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4;
   // packed tile of one k-block (BF16: the operand tile itself, already swizzled by TMA)
@@ -122,8 +122,13 @@ struct Fmt {
   static constexpr int kPUnitBytes = kUnitKb * kPStageBytes;
   // Units of the packed ring.  Like the other rings it moves in units that both dequant
   // teams consume in order, so no parity wait can alias a phase two laps away.
-  static constexpr int kPUnits = FMT == BSQ_BF16 ? 1 : (FMT == BSQ_FP8_E4M3_B128 ? 2 : 3);
-  static constexpr int kRingBytes = kUStages * (kBUnitBytes + kAUnitBytes) + kPUnits * kPUnitBytes;
+  // The short-tile kernel of an FP4 format stages each epilogue warp's 16 x 32 output
+  // chunk in shared memory for a TMA store, paid for with one packed unit.
+  static constexpr bool kEpiStaged = SHORT && kFp4;
+  static constexpr int kPUnits = (FMT == BSQ_BF16 ? 1 : (FMT == BSQ_FP8_E4M3_B128 ? 2 : 3)) - (kEpiStaged ? 1 : 0);
+  static constexpr int kEpiStage = 1024;                                 // [16 n][32 m] BF16 per epilogue warp
+  static constexpr int kEpiBytes = kEpiStaged ? Roles<true>::kEpiWarps * kEpiStage : 0;
+  static constexpr int kRingBytes = kUStages * (kBUnitBytes + kAUnitBytes) + kPUnits * kPUnitBytes + kEpiBytes;
 };
 
 struct Params {
@@ -290,6 +295,7 @@ struct OpArgs {
   CUtensorMap tm_p;
   CUtensorMap tm_g;
   CUtensorMap tm_s;
+  CUtensorMap tm_o;
   Params p;
 };
 
@@ -317,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bsq_gemm_kernel(const __grid_constant__ CUtensorMap tm_p0, const __grid_constant__ CUtensorMap tm_g0,
                     const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_p1,
                     const __grid_constant__ CUtensorMap tm_g1, const __grid_constant__ CUtensorMap tm_s1,
-                    const Params p, const Params p1) {
-  using F = Fmt<FMT>;
+                    const __grid_constant__ CUtensorMap tm_o, const Params p, const Params p1) {
+  using F = Fmt<FMT, SHORT>;
   using R = Roles<SHORT>;
   constexpr int OP0 = OPS == kBoth ? static_cast<int>(kDgrad) : OPS;
   static_assert(!SHORT || FMT != BSQ_BF16, "the short-tile kernel decodes packed formats only");
@@ -330,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring_b = smem;
   uint8_t* ring_a = ring_b + kUStages * kBUnitBytes;
   uint8_t* ring_p = ring_a + kUStages * kAUnitBytes;
+  uint8_t* ring_e = ring_p + F::kPUnits * F::kPUnitBytes;
   SharedTail& sh = *reinterpret_cast<SharedTail*>(smem + F::kRingBytes);
   volatile uint32_t* abort_flag = &sh.abort_flag;
 
@@ -609,6 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = R::kEpiPerQuarter > 1 ? (warp - 4) >> 2 : 0;   // 0 .. kEpiPerQuarter-1
     const int i = q * 32 + lane;              // accumulator row = tile m index (permuted)
     const int mcol = lane_to_col<FMT>(i);
+    const int lm = mcol - q * 32;             // column inside the warp's 32
+    const uint32_t estage = smem_u32(ring_e) + (warp - 4) * F::kEpiStage;
     ExpertCursor c0 = cursor_begin<OP0>(p), c1 = cursor_begin<kWgrad>(p1);
     uint32_t acc = 0;
     for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
@@ -623,10 +632,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         obase += ti.e * pick(second, p.out_expert_stride, p1.out_expert_stride) +
                  static_cast<int64_t>(ti.nt * kTileN) * p.Kc + m;
       if (ti.kblocks == 0) {
-        // wgrad of an expert without rows: exact zeros
-        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-        if (mok)
-          for (int n = sub; n < ti.n_valid; n += R::kEpiPerQuarter) obase[static_cast<int64_t>(n) * p.Kc] = z;
+        // wgrad of an expert without rows: exact zeros, 16 bytes per lane, 8 rows per warp store
+        const int zc = ti.mt * kTileM + q * 32 + (lane & 3) * 8;
+        __nv_bfloat16* zrow = pick(second, p.out, p1.out) + ti.e * pick(second, p.out_expert_stride, p1.out_expert_stride) +
+                              static_cast<int64_t>(ti.nt * kTileN) * p.Kc + zc;
+        if (zc < p.Kc)
+          for (int n = (lane >> 2) + 8 * sub; n < ti.n_valid; n += 8 * R::kEpiPerQuarter)
+            *reinterpret_cast<uint4*>(zrow + static_cast<int64_t>(n) * p.Kc) = make_uint4(0u, 0u, 0u, 0u);
         continue;
       }
       const uint32_t buf = acc & 1u;
@@ -662,7 +674,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t h[8];   // (n, n+1) pairs of this thread's column m, BF16
 #pragma unroll
         for (int j = 0; j < 8; ++j) h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-        if (mok) {
+        if (F::kEpiStaged) {
+          // [16 n][32 m] BF16 through this warp's staging area, then one TMA store (rows and
+          // columns outside the output are clipped by the tensor map)
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            sts_u16(estage + j * 64 + lm * 2, (j & 1) ? (h[j >> 1] >> 16) : (h[j >> 1] & 0xFFFFu));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && ti.mt * kTileM + q * 32 < p.Kc) {
+            tma_store_3d(&tm_o, estage, ti.mt * kTileM + q * 32, ti.nt * kTileN + c * 16, ti.e);
+            bulk_commit();
+          }
+        } else if (mok) {
           const int nlim = min(16, ti.n_valid - c * 16);
           const int64_t step = p.Kc;
           unsigned short* o = reinterpret_cast<unsigned short*>(obase) + static_cast<int64_t>(c * 16) * step;
@@ -673,6 +699,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    }
+    if (F::kEpiStaged) {
+      if (lane == 0) bulk_wait_all0();
+      __syncwarp();
     }
   } else if (warp >= R::kFirstDeq) {
     // ===== dequantization =====
@@ -785,6 +815,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[jj][0] = c.x; v[jj][1] = c.y; v[jj][2] = c.z; v[jj][3] = c.w;
           }
         }
+        // The producer refills this slot by TMA (the async proxy) once every dequant warp has
+        // arrived; this lane's plain loads from it must be performed first.  Without the fence
+        // nothing orders them, and a load still queued behind other shared-memory traffic of
+        // the SM can read the next unit's bytes.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));   // this warp is done with the packed slot
         // ---- decode the first row into registers while the operand slot may still be busy
@@ -970,6 +1005,17 @@ int prepare_op(const GemmArgs& a, OpArgs& o, int64_t* bound, const char** msg) {
       return -1;
     }
   }
+  // wgrad output [E][N][Kc] as TMA store boxes of 16 rows x 32 columns
+  o.tm_o = o.tm_p;
+  if (!dgrad) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(a.kc), static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(a.kc) * 2, static_cast<uint64_t>(a.kc * a.N) * 2};
+    const uint32_t box[3] = {32, 16, 1};
+    if (!encode_map(&o.tm_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      *msg = "tensor map encoding failed for the output";
+      return -1;
+    }
+  }
   // FP4 scale tiles through TMA when the scale row pitch is a multiple of 16 bytes.
   o.tm_s = o.tm_p;
   int scale_tma = 0;
@@ -1027,7 +1073,6 @@ int prepare_op(const GemmArgs& a, OpArgs& o, int64_t* bound, const char** msg) {
 // (OPS = kBoth; ops[0] the dgrad, ops[1] the wgrad).
 template <int FMT, int OPS>
 int launch_typed(const GemmArgs* ops, const char** msg) {
-  using F = Fmt<FMT>;
   OpArgs a0, a1;
   int64_t b0 = 0, b1 = 0;
   if (prepare_op<FMT>(ops[0], a0, &b0, msg) != 0) return -1;
@@ -1038,8 +1083,9 @@ int launch_typed(const GemmArgs* ops, const char** msg) {
   }
   const int64_t bound = b0 + b1;
   const GemmArgs& a = ops[0];
-  static_assert(F::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
-  const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(SharedTail) + 1024;
+  static_assert(Fmt<FMT>::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
+  static_assert(Fmt<FMT, true>::kRingBytes + sizeof(SharedTail) + 1024 <= 232448, "rings exceed the 227 KB of shared memory per CTA");
+  size_t smem = static_cast<size_t>(Fmt<FMT>::kRingBytes) + sizeof(SharedTail) + 1024;
   // Kernel: wgrad of a packed format whose groups average fewer than 1024 rows (a tile of
   // at most 16 k-blocks, where the epilogue sets the pace) takes the short-tile variant
   // (more epilogue warps).  BSQ_GEMM_SHORT_TILES=1 / 0 forces one or the other.
@@ -1049,7 +1095,10 @@ int launch_typed(const GemmArgs* ops, const char** msg) {
     const char* env = std::getenv("BSQ_GEMM_SHORT_TILES");
     if (env && (env[0] == '0' || env[0] == '1')) short_tiles = env[0] == '1';
     else short_tiles = a.S < 1024 * a.E;
-    if (short_tiles) kern = bsq_gemm_kernel<FMT, OPS, true>;
+    if (short_tiles) {
+      kern = bsq_gemm_kernel<FMT, OPS, true>;
+      smem = static_cast<size_t>(Fmt<FMT, true>::kRingBytes) + sizeof(SharedTail) + 1024;
+    }
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -1083,7 +1132,7 @@ int launch_typed(const GemmArgs* ops, const char** msg) {
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kPair));
   if (e == cudaSuccess)
-    e = cudaLaunchKernelEx(&cfg, kern, a0.tm_p, a0.tm_g, a0.tm_s, a1.tm_p, a1.tm_g, a1.tm_s, a0.p, a1.p);
+    e = cudaLaunchKernelEx(&cfg, kern, a0.tm_p, a0.tm_g, a0.tm_s, a1.tm_p, a1.tm_g, a1.tm_s, a0.tm_o, a0.p, a1.p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);

@@ -708,14 +708,16 @@ __global__ void __launch_bounds__(kThreadsSm, 2)
         }
         // This warp is done with the chunk's slot (its reads are in registers and consumed).
         // The fourth warp of the group to let it go refills it with the chunk kRing later:
-        // nobody waits for a slot to drain.
+        // nobody waits for a slot to drain.  Every lane orders its plain reads of the slot
+        // before the copy (the async proxy) that overwrites it.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           __threadfence_block();
           const uint32_t prior = atomicAdd(&released[si], 1u);
           if ((prior & 3u) == 3u && c + kRing < nchunks) {
             __threadfence_block();
-            fence_proxy_async_smem();   // the slot's plain reads come before the copy that overwrites it
+            fence_proxy_async_smem();
             issue(cc + kRing, c + kRing, e, r0);
           }
         }
