@@ -12,6 +12,12 @@ is fixed, so each repeat must equal the first run bit for bit over the whole out
 Workloads: MXFP4 4096^3 dense dgrad and wgrad, as one fused backward launch and as the two
 single-product launches, and the 128-expert MXFP4 grouped dgrad and wgrad (Dirichlet(0.3)
 routing, empty experts; its wgrad takes the short-tile kernel).
+
+A second test repeats the grouped workloads while another stream copies 2 GB buffers, so
+that the kernels' loads meet a busy memory system at varying moments.  A result that
+depends on when a load completes relative to the refill of its buffer (a ring slot read
+with plain loads and refilled by TMA without an order between the two) differs from the
+clean run there.
 """
 
 import pytest
@@ -53,3 +59,33 @@ def test_repeats_match_oracle_and_first_run(cfg, fused):
     st, code = bsq.get_device_error()
     assert st == bsq.BSQ_OK and code == 0, (st, code)
     assert not bad, f"{c['name']}: repeats that differ from the first run (rep, op, elements): {bad}"
+
+
+@pytest.mark.parametrize("n", [4, 5])
+def test_repeats_under_concurrent_memory_traffic_match_first_run(n):
+    c = synth.make_config(n, device="cuda")
+    first = run_config(c)
+    ref = {k: v.clone() for k, v in first.items()}
+    src = torch.empty(1 << 31, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    side = torch.cuda.Stream()
+    bad = []
+    for rep in range(6):
+        for v in first.values():
+            v.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            for _ in range(1 + rep % 3):
+                dst.copy_(src)
+                src.copy_(dst)
+        if rep % 2:
+            torch.cuda._sleep(20000 * rep)   # vary where the copies overlap the launch
+        run_config(c, first)
+        for k, v in first.items():
+            if not torch.equal(v.view(torch.int16), ref[k].view(torch.int16)):
+                bad.append((rep, k, int((v.view(torch.int16) != ref[k].view(torch.int16)).sum().item())))
+    torch.cuda.synchronize()
+    del src, dst
+    st, code = bsq.get_device_error()
+    assert st == bsq.BSQ_OK and code == 0, (st, code)
+    assert not bad, f"{c['name']}: repeats under concurrent traffic that differ from the clean run: {bad}"
