@@ -9,9 +9,9 @@
 //        bytes of BF16.  (16-byte loads of 32 codes per lane leave each lane a 64-byte run
 //        of output, so every store instruction scatters half sectors: measured at about
 //        half the bandwidth.)  Scales: one E8M0 / E4M3 byte per 8 codes.
-//   FP8: every lane reads 16-byte loads of 16 codes of one row (two in flight) and writes
-//        two 16-byte stores; one scale_inv per load (a load never crosses a 128-column
-//        scale block), its index formed once per 16 codes.
+//   FP8: blocks walk whole rows; consecutive lanes take consecutive 8-code units of a row
+//        (8-byte loads, 16-byte stores, warp-contiguous), four rows in flight, and the
+//        scale-block row is carried from row to row instead of divided out per unit.
 #include <cuda_bf16.h>
 
 #include "bsq_decode.cuh"
@@ -88,45 +88,72 @@ __global__ void __launch_bounds__(kThreads) dequant_fp4_kernel(const uint32_t* _
   }
 }
 
-// FP8 E4M3, 16-byte form: one uint4 = 16 codes of one row (cols % 16 == 0, so a load never
-// crosses a row or a 128-column scale block) = 2 output uint4, two loads in flight.
-__global__ void __launch_bounds__(kThreads) dequant_fp8_x2_kernel(const uint4* __restrict__ data,
-                                                                  const float* __restrict__ scale_inv,
-                                                                  int64_t n_pairs, int64_t rows, int64_t cols,
-                                                                  int shift, uint4* __restrict__ out) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  const int64_t per_row = cols >> 4;
+// FP8 E4M3, row walk: block b takes the rows b, b + G, ... of the whole batch (G = grid
+// size), four at a time; thread t takes the 8-code units t, t + 256, ... of each row, so a
+// warp reads 256 and writes 512 contiguous bytes per instruction, four rows' loads in
+// flight.  A row's batch entry and scale-block row are carried from step to step (a
+// division only when a step passes more than one batch entry), one scale_inv per 8 codes.
+__global__ void __launch_bounds__(kThreads) dequant_fp8_rows_kernel(const uint2* __restrict__ data,
+                                                                    const float* __restrict__ scale_inv,
+                                                                    int64_t total_rows, int64_t rows, int64_t cols,
+                                                                    int shift, uint4* __restrict__ out) {
+  const int64_t per_row = cols >> 3;
   const int64_t rblocks = shift >= 31 ? 1 : (rows + (1 << shift) - 1) >> shift;
   const int64_t cblocks = shift >= 31 ? 1 : (cols + (1 << shift) - 1) >> shift;
-  auto scale_of = [&](int64_t i) {
-    const int64_t grow = i / per_row;               // row across the whole batch
-    const int64_t col = (i - grow * per_row) << 4;
-    const int64_t b = grow / rows;
-    const int64_t r = grow - b * rows;
-    return __ldg(scale_inv + (b * rblocks + (r >> shift)) * cblocks + (col >> shift));
-  };
-  auto put = [&](const uint4& w, float sv, int64_t i) {
-    const ScaleBf16 s = make_scale_fp8(sv);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t a02, a13, b02, b13;
-      decode_e4m3x4(ws[2 * h], s, a02, a13);
-      decode_e4m3x4(ws[2 * h + 1], s, b02, b13);
-      uint4 o;
-      unzip_pairs(a02, a13, o.x, o.y);  // (c0,c1), (c2,c3)
-      unzip_pairs(b02, b13, o.z, o.w);  // (c4,c5), (c6,c7)
-      out[2 * i + h] = o;
+  const int64_t G = gridDim.x;
+  // (batch entry, row inside it) of global row g, carried forward by `by` rows
+  auto step = [&](int64_t& b, int64_t& r, int64_t by) {
+    r += by;
+    if (r >= rows) {
+      if (r < 2 * rows) {   // the usual case: at most one batch entry passed
+        r -= rows;
+        ++b;
+      } else {
+        b += r / rows;
+        r %= rows;
+      }
     }
   };
-  int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  for (; i + stride < n_pairs; i += 2 * stride) {
-    const uint4 wa = __ldg(data + i), wb = __ldg(data + i + stride);
-    const float sa = scale_of(i), sb = scale_of(i + stride);
-    put(wa, sa, i);
-    put(wb, sb, i + stride);
+  int64_t b0 = static_cast<int64_t>(blockIdx.x) / rows, r0 = static_cast<int64_t>(blockIdx.x) - b0 * rows;
+  for (int64_t row = blockIdx.x; row < total_rows; row += 4 * G, step(b0, r0, 4 * G)) {
+    int64_t bb[4], rr[4];
+    bb[0] = b0;
+    rr[0] = r0;
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+      bb[k] = bb[k - 1];
+      rr[k] = rr[k - 1];
+      step(bb[k], rr[k], G);
+    }
+    for (int64_t u = threadIdx.x; u < per_row; u += kThreads) {
+      const int64_t cb = (u << 3) >> shift;
+      uint2 w[4];
+      float sv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t grow = row + k * G;
+        w[k] = make_uint2(0u, 0u);
+        sv[k] = 0.f;
+        if (grow < total_rows) {
+          w[k] = __ldg(data + grow * per_row + u);
+          sv[k] = __ldg(scale_inv + (bb[k] * rblocks + (rr[k] >> shift)) * cblocks + cb);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t grow = row + k * G;
+        if (grow >= total_rows) continue;
+        const ScaleBf16 s = make_scale_fp8(sv[k]);
+        uint32_t a02, a13, b02, b13;
+        decode_e4m3x4(w[k].x, s, a02, a13);
+        decode_e4m3x4(w[k].y, s, b02, b13);
+        uint4 o;
+        unzip_pairs(a02, a13, o.x, o.y);  // (c0,c1), (c2,c3)
+        unzip_pairs(b02, b13, o.z, o.w);  // (c4,c5), (c6,c7)
+        out[grow * per_row + u] = o;
+      }
+    }
   }
-  if (i < n_pairs) put(__ldg(data + i), scale_of(i), i);
 }
 
 }  // namespace
@@ -139,19 +166,18 @@ int launch_dequant(const DequantArgs& a, const char** msg) {
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
   if (blocks > cap) blocks = cap;
   const dim3 grid(static_cast<unsigned>(blocks)), block(kThreads);
-  // FP8: the 16-byte form (one 16-byte load per lane per step, two steps in flight)
+  // FP8: the row walk, one block per row at a time (eight resident blocks per SM)
   if (a.fmt == BSQ_FP8_E4M3_B128 || a.fmt == BSQ_FP8_E4M3_TENSOR) {
-    const int64_t loads = elems / 16;
-    int64_t b16 = (loads + 2 * kThreads - 1) / (2 * kThreads);
-    const int64_t cap16 = static_cast<int64_t>(a.num_sms) * 8;
-    b16 = b16 < 1 ? 1 : (b16 > cap16 ? cap16 : b16);
-    dequant_fp8_x2_kernel<<<dim3(static_cast<unsigned>(b16)), block, 0, a.stream>>>(
-        static_cast<const uint4*>(a.data), static_cast<const float*>(a.scale), loads, a.rows, a.cols,
+    const int64_t trows = a.batch * a.rows;
+    int64_t g = static_cast<int64_t>(a.num_sms) * 8;
+    if (g > trows) g = trows;
+    dequant_fp8_rows_kernel<<<dim3(static_cast<unsigned>(g)), block, 0, a.stream>>>(
+        static_cast<const uint2*>(a.data), static_cast<const float*>(a.scale), trows, a.rows, a.cols,
         fp8_scale_shift(a.fmt), static_cast<uint4*>(a.out));
-    const cudaError_t e16 = cudaGetLastError();
-    if (e16 != cudaSuccess) {
-      *msg = cudaGetErrorString(e16);
-      return static_cast<int>(e16);
+    const cudaError_t ef = cudaGetLastError();
+    if (ef != cudaSuccess) {
+      *msg = cudaGetErrorString(ef);
+      return static_cast<int>(ef);
     }
     return 0;
   }
