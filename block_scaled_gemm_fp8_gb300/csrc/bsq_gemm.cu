@@ -26,14 +26,16 @@
 //   warp 2      allocates / frees TMEM; one lane relays "operand ready" to the even CTA
 //   warp 3      TMA producer of the grad_out ring: this CTA's half of the unit's tiles
 //   warp 1      MMA issuer, one thread of the even CTA: 4 x (256 x Nm x 16) per k-block
-//   warps 4-7   epilogue: tcgen05.ld (pipelined, 16 columns at a time) -> BF16 -> global,
-//               one TMEM lane quarter each
+//   warps 4-7   epilogue: tcgen05.ld (16 columns at a time, each load waited for in the
+//               same statement) -> BF16 -> global, one TMEM lane quarter each; the FP4
+//               short-tile kernel stages each chunk in shared memory for a TMA store
 //   warps 8-23  dequantization, two teams of 8 warps; team t takes k-block t of every
 //               unit: packed codes (smem) -> BF16, written in the 128-byte swizzled
 //               MN-major layout the tensor core reads; also zero the rows of a k-block
 //               that lie outside the current expert (wgrad)
-// Three rings decouple the chains: the packed ring feeds the dequant teams; the BF16
-// operand ring feeds the MMA from the dequant teams; the grad_out ring feeds the MMA
+// Three rings decouple the chains: the packed ring feeds the dequant teams (plain loads,
+// fenced against the async proxy before each slot goes back to its TMA producer); the
+// BF16 operand ring feeds the MMA from the dequant teams; the grad_out ring feeds the MMA
 // straight from TMA.  All three move in units of two k-blocks, and every barrier phase
 // of a ring is waited on by the same threads in unit order (a parity wait cannot then
 // mistake a phase two laps away for its own).  The operand and grad_out rings share
