@@ -159,3 +159,56 @@ def test_grouped_wgrad_one_hot_edge_scales(fmt, kind, short, monkeypatch):
         else:
             assert_bits(out[e], expected_one_hot(x[r0:r1], picks[e]), f"grouped wgrad e={e} fmt={fmt} {kind}")
     assert bsq.get_device_error() == (bsq.BSQ_OK, 0)
+
+
+# ---- the small-M kernels (their own decode): M <= 16 linear dgrad, decode-sized grouped dgrad
+
+
+@pytest.mark.parametrize("M", [1, 9, 16])
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("fmt", PACKED)
+def test_small_m_dgrad_one_hot_edge_scales(fmt, kind, M):
+    N, K = 200, 384       # ragged contraction over three 64-row chunks, three 128-column slabs
+    W = synth.random_codes(fmt, 1, N, K, seed=340 + fmt, scale_kind=kind)
+    G, picks = _one_hot_rows(M, N, 341 + M)
+    out = bsq.linear_dgrad(G.cuda(), W.to("cuda"))
+    torch.cuda.synchronize()
+    assert_bits(out, expected_one_hot(oracle_deq(W)[0], picks), f"small-M dgrad M={M} fmt={fmt} {kind}")
+    assert bsq.get_device_error() == (bsq.BSQ_OK, 0)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("fmt", [synth.FMT_FP8, synth.FMT_MXFP4, synth.FMT_NVFP4])   # the formats it takes
+def test_small_m_noalloc_one_hot_edge_scales(fmt, kind):
+    M, N, K = 12, 200, 384
+    W = synth.random_codes(fmt, 1, N, K, seed=350 + fmt, scale_kind=kind)
+    G, picks = _one_hot_rows(M, N, 351)
+    out = bsq.linear_dgrad_smallm_noalloc(G.cuda(), W.to("cuda"))
+    torch.cuda.synchronize()
+    assert_bits(out, expected_one_hot(oracle_deq(W)[0], picks), f"noalloc small-M dgrad fmt={fmt} {kind}")
+    assert bsq.get_device_error() == (bsq.BSQ_OK, 0)
+
+
+DECODE_COUNTS = [3, 0, 20, 1, 30]   # 54 rows in all: the decode-sized grouped path
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("fmt", PACKED)
+def test_grouped_decode_one_hot_edge_scales(fmt, kind):
+    N, K = 200, 384
+    E = len(DECODE_COUNTS)
+    offs = synth.offsets_from_counts(DECODE_COUNTS)
+    S = int(offs[-1]) + 5
+    W = synth.random_codes(fmt, E, N, K, seed=360 + fmt, scale_kind=kind)
+    G, picks = _one_hot_rows(S, N, 361)
+    out = torch.full((S, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bsq.grouped_dgrad(G.cuda(), W.to("cuda"), torch.from_numpy(offs).cuda(), out=out)
+    torch.cuda.synchronize()
+    w = oracle_deq(W)
+    for e in range(E):
+        r0 = 0 if e == 0 else int(offs[e - 1])
+        r1 = int(offs[e])
+        if r1 > r0:
+            assert_bits(out[r0:r1], expected_one_hot(w[e], picks[r0:r1]), f"decode dgrad e={e} fmt={fmt} {kind}")
+    assert torch.isnan(out[int(offs[-1]):].float()).all()
+    assert bsq.get_device_error() == (bsq.BSQ_OK, 0)
