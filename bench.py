@@ -51,7 +51,7 @@ def parse_args():
                     help="time only the headline workload (not the other four, nor the standalone dequant)")
     ap.add_argument("--profile", default=None,
                     choices=["backward", "dgrad", "wgrad", "grouped_dgrad", "grouped_wgrad", "small_m", "dequant",
-                             "forward", "e5m2"],
+                             "forward", "forward_bf16", "e5m2"],
                     help="run only this op of the workload, --warmup + --steps times back to back, and print "
                          "its mean time (a fixed launch sequence for ncu; not a benchmark line)")
     ap.add_argument("--experts", type=int, default=None,
@@ -80,9 +80,10 @@ def profile_run(args, bsq, synth, dev):
         f = lambda: bsq.grouped_dgrad(c["G"], c["W"], c["offsets_dev"], out=outs["grouped_dgrad"])
     elif op == "grouped_wgrad":
         f = lambda: bsq.grouped_wgrad(c["G"], c["X"], c["offsets_dev"], c["E"], out=outs["grouped_wgrad"])
-    elif op == "forward":
+    elif op in ("forward", "forward_bf16"):
         yo = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
-        f = lambda: bsq.linear_forward(c["X"], c["W"], out=yo)
+        xf = c["X"] if op == "forward" else synth.make_packed(synth.FMT_BF16, 1, c["M"], c["K"], 1.0, 77, dev)
+        f = lambda: bsq.linear_forward(xf, c["W"], out=yo)
     elif op == "e5m2":
         qc = torch.empty(c["G"].shape, dtype=torch.uint8, device=dev)
         qd = torch.empty(c["G"].shape, dtype=torch.bfloat16, device=dev)
@@ -494,7 +495,7 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     r["frac_burst"] = r["tflops"] / pk["bf16_tflops"]
     r["frac_sustained"] = r["tflops"] / pk["bf16_tflops_sustained"]
     if not c["grouped"] and c["X"].fmt != 0:
-        r["forward"] = measure_forward(c, bsq, steps, warmup, flush, pk)
+        r["forward"] = measure_forward(c, bsq, synth, steps, warmup, flush, pk)
     if n in SMALL_M_WORKLOADS:
         # M = 16 token rows against this workload's weight as well (the split-K kernel)
         if "G_small" not in c:
@@ -512,29 +513,38 @@ def measure_workload(n, bsq, synth, dev, steps, warmup, flush, pk):
     return r, deq
 
 
-def measure_forward(c, bsq, steps, warmup, flush, pk):
-    """bsq_linear_forward (Y = X W^T, both packed) on the workload's X and W."""
+def measure_forward(c, bsq, synth, steps, warmup, flush, pk):
+    """bsq_linear_forward (Y = X W^T) on the workload's packed X and W, and with a BF16 X of
+    the same shape (a layer whose weight alone is quantized) under "bf16_activation"."""
     y = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=c["G"].device)
-    for _ in range(warmup):
-        bsq.linear_forward(c["X"], c["W"], out=y)
-    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    ts = []
-    for _ in range(steps):
-        flush.zero_()
-        torch.cuda._sleep(HOST_COVER_CYCLES)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        bsq.linear_forward(c["X"], c["W"], out=y)
-        b.record(stream)
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    ms = statistics.median(ts)
     M, N, K = c["M"], c["N"], c["K"]
     fl = 2.0 * M * N * K
-    nb = packed_bytes(c["X"]) + packed_bytes(c["W"]) + 2.0 * M * N
-    r = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "roofline": op_roofline(fl, nb, ms, pk)}
+
+    def timed(X):
+        for _ in range(warmup):
+            bsq.linear_forward(X, c["W"], out=y)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            torch.cuda._sleep(HOST_COVER_CYCLES)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bsq.linear_forward(X, c["W"], out=y)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        nb = packed_bytes(X) + packed_bytes(c["W"]) + 2.0 * M * N
+        return {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "roofline": op_roofline(fl, nb, ms, pk)}
+
+    r = timed(c["X"])
     r["roofline"]["traffic"] = profiled_traffic(c["name"], "forward")
+    xb = synth.make_packed(synth.FMT_BF16, 1, M, K, 1.0, 77, y.device)
+    r["bf16_activation"] = timed(xb)
+    r["bf16_activation"]["roofline"]["traffic"] = profiled_traffic(c["name"], "forward_bf16_activation")
+    del xb
     return r
 
 
@@ -801,7 +811,7 @@ def main():
             "roofline": roof, "gpu_launches": launches, "clocks": clocks}
 
     if not c["grouped"] and c["X"].fmt != 0:
-        line["forward"] = measure_forward(c, bsq, args.steps, args.warmup, flush, pk)
+        line["forward"] = measure_forward(c, bsq, synth, args.steps, args.warmup, flush, pk)
     if args.config == 2:
         ms, nbytes = time_small_m(c, bsq, args.steps, args.warmup, flush)
         line["small_m_dgrad"] = {"M": int(c["G_small"].shape[0]), "ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,

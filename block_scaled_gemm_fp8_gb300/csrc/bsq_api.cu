@@ -314,16 +314,16 @@ bsq_status bsq_linear_forward(int32_t x_fmt, const void* x_data, const void* x_s
                               const float* w_tensor_scale, int64_t N, int64_t K, void* y, void* stream) {
   const char* what = "bsq_linear_forward";
   if (M < 0 || N < 0 || K < 0) return fail(BSQ_ERR_INVALID_ARG, "%s: negative size", what);
-  bsq_status st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, false);
+  bsq_status st = check_packed(what, x_fmt, x_data, x_scale, x_tensor_scale, 1, M, K, true);
   if (st != BSQ_OK) return st;
   st = check_packed(what, w_fmt, w_data, w_scale, w_tensor_scale, 1, N, K, false);
   if (st != BSQ_OK) return st;
   if (x_fmt == BSQ_FP8_E5M2_TENSOR || w_fmt == BSQ_FP8_E5M2_TENSOR)
     return fail(BSQ_ERR_UNSUPPORTED, "%s: E5M2 is the gradient's format, not an operand's", what);
-  if (bsq::kernel_fmt(x_fmt) != bsq::kernel_fmt(w_fmt))
+  if (x_fmt != BSQ_BF16 && bsq::kernel_fmt(x_fmt) != bsq::kernel_fmt(w_fmt))
     return fail(BSQ_ERR_UNSUPPORTED, "%s: X and W must share a packed format (FP8 blocks and per-tensor mix)", what);
   if (N % 8) return fail(BSQ_ERR_UNSUPPORTED, "%s: N %% 8 != 0 (Y row pitch must be 16 bytes)", what);
-  if (x_fmt == BSQ_NVFP4 && K % 32)
+  if ((x_fmt == BSQ_NVFP4 || w_fmt == BSQ_NVFP4) && K % 32)
     return fail(BSQ_ERR_UNSUPPORTED, "%s: NVFP4 K %% 32 != 0 (packed row pitch must be 16 bytes)", what);
   if (M * N > 0 && (!y || !aligned16(y))) return fail(BSQ_ERR_INVALID_ARG, "%s: Y null or not 16-byte aligned", what);
   if (M == 0 || N == 0) return BSQ_OK;

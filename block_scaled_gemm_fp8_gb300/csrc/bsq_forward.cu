@@ -1,5 +1,5 @@
-// bsq_forward.cu -- the forward product of a block-scaled linear layer, with both operands
-// packed:  Y[M, N] = deq(X)[M, K] @ deq(W)[N, K]^T  (BF16 out, FP32 accumulation).
+// bsq_forward.cu -- the forward product of a block-scaled linear layer, W packed and X packed
+// or BF16:  Y[M, N] = deq(X)[M, K] @ deq(W)[N, K]^T  (BF16 out, FP32 accumulation).
 //
 // This is the op whose backward the rest of the library computes: MSLK PR #393 adds the
 // backward of its FP4 GEMM ops (`mslk::f4f4bf16` and the grouped forms), whose forward
@@ -15,16 +15,25 @@
 // are unchanged.  Output rows are contiguous along the accumulator's columns, so the
 // epilogue writes 16-byte stores.
 //
+// X may also be given in BF16 (the layer of the FP8 linear workload has a BF16 activation
+// and an FP8 weight).  Then TMA brings X's K-major tiles straight into the A ring, 128-byte
+// swizzled exactly as the decode would have written them, and the dequant warps decode W
+// alone, storing each group of 8 k in natural order so that it lines up with X's elements.
+//
 // Per CTA, 24 warps (one CTA per SM, clusters of two):
-//   warp 0      TMA producer: packed X and W tiles of each k-block
+//   warp 0      TMA producer: packed X and W tiles of each k-block (BF16 X: W's only)
 //   warp 1      MMA issuer, one thread of the even CTA
 //   warp 2      TMEM allocation; one lane relays "operands ready" to the even CTA
+//   warp 3      BF16 X: TMA producer of X's tiles, into the A ring once the MMA has
+//               released the slot
 //   warps 4-7   epilogue
 //   warps 8-23  dequantization, two teams of 8 warps (team t: k-block t of every unit);
-//               each thread decodes 32 k of one row of X and 32 k of one row of W
+//               each thread decodes 32 k of one row of X (packed X only) and 32 k of one
+//               row of W
 // The pair protocol is the backward kernel's: a CTA-local barrier per unit for the
-// dequant warps, then the even relay's arrival and the odd relay's st.async (a release at
-// cluster scope) on the even CTA's barrier, which the MMA thread acquires at cluster scope.
+// dequant warps (and, for a BF16 X, the barrier its TMA tiles complete on), then the even
+// relay's arrival and the odd relay's st.async (a release at cluster scope) on the even
+// CTA's barrier, which the MMA thread acquires at cluster scope.
 #include <atomic>
 #include <cstdlib>
 
@@ -52,20 +61,23 @@ constexpr int kKb = 64;                            // k per k-block
 constexpr int kNTile = 256;                        // n per pair tile
 constexpr int kOpBytes = kRowsF * kKb * 2;         // 16 KB: one decoded K-major tile (128 rows x 128 bytes)
 constexpr int kUnit = 2;                           // k-blocks per unit
-constexpr int kOpStages = 2;                       // units of the decoded rings
+constexpr int kMaxOpStages = 3;
 constexpr int kOpUnitBytes = kUnit * kOpBytes;     // 32 KB per operand
 constexpr int kTmemColsF = 512;
 constexpr int kDeqWarpsF = 16;
 constexpr int kFirstDeqF = 8;
 
-template <int FMT>
+// FMT: W's format (and X's when packed); XBF: X is BF16.
+template <int FMT, bool XBF>
 struct FwdFmt {
   static constexpr bool kFp4 = FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4;
   static constexpr int kRowBytes = kFp4 ? kKb / 2 : kKb;          // packed bytes of one row's k-block
   static constexpr int kTileBytes = kRowsF * kRowBytes;            // one packed tile (X or W half)
-  static constexpr int kStageBytes = 2 * kTileBytes;               // X tile + W tile of a k-block
+  static constexpr int kStageBytes = (XBF ? 1 : 2) * kTileBytes;   // (X tile +) W tile of a k-block
   static constexpr int kUnitBytes = kUnit * kStageBytes;
   static constexpr int kPUnits = kFp4 ? 3 : 2;
+  static constexpr int kOpStages = XBF ? 3 : 2;                    // units of the operand rings
+  static_assert(kOpStages <= kMaxOpStages, "barrier arrays");
   static constexpr int kRingBytes = 2 * kOpStages * kOpUnitBytes + kPUnits * kUnitBytes;
 };
 
@@ -88,9 +100,10 @@ struct FwdParams {
 struct FwdShared {
   uint64_t p_full[4];
   uint64_t p_empty[4];
-  uint64_t a_local[kOpStages];
-  uint64_t a_full[kOpStages];
-  uint64_t op_empty[kOpStages];
+  uint64_t a_local[kMaxOpStages];
+  uint64_t a_full[kMaxOpStages];
+  uint64_t op_empty[kMaxOpStages];
+  uint64_t x_full[kMaxOpStages];   // BF16 X: the A ring's TMA tiles have landed
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t drain;
@@ -150,16 +163,40 @@ __device__ __forceinline__ void decode32(const uint4& wa, const uint4& wb, uint3
   }
 }
 
+// decode32's groups back in natural k order: the E2M1 spread gives pairs (e_i, e_i+4), the
+// E4M3 one (c_0, c_2), (c_1, c_3) per word; a BF16 X operand holds its k in order.
 template <int FMT>
+__device__ __forceinline__ void natural_order(uint32_t (&v)[4][4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint32_t l0, h0, l1, h1;
+    unzip_pairs(v[g][0], v[g][1], l0, h0);
+    unzip_pairs(v[g][2], v[g][3], l1, h1);
+    if (FMT == BSQ_MXFP4 || FMT == BSQ_NVFP4) {
+      v[g][0] = l0;   // (e0, e1)
+      v[g][1] = l1;   // (e2, e3)
+      v[g][2] = h0;   // (e4, e5)
+      v[g][3] = h1;   // (e6, e7)
+    } else {
+      v[g][0] = l0;   // (c0, c1)
+      v[g][1] = h0;   // (c2, c3)
+      v[g][2] = l1;   // (c4, c5)
+      v[g][3] = h1;   // (c6, c7)
+    }
+  }
+}
+
+template <int FMT, bool XBF>
 __global__ void __launch_bounds__(kThreadsF, 1)
     bsq_forward_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const FwdParams p) {
-  using F = FwdFmt<FMT>;
+  using F = FwdFmt<FMT, XBF>;
+  constexpr int kOpStages = F::kOpStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring_a = smem;                                   // decoded X tiles (A)
+  uint8_t* ring_a = smem;                                   // X tiles (A): decoded, or BF16 by TMA
   uint8_t* ring_b = ring_a + kOpStages * kOpUnitBytes;      // decoded W tiles (B, this CTA's half)
-  uint8_t* ring_p = ring_b + kOpStages * kOpUnitBytes;      // packed X and W tiles
+  uint8_t* ring_p = ring_b + kOpStages * kOpUnitBytes;      // packed (X and) W tiles
   FwdShared& sh = *reinterpret_cast<FwdShared*>(smem + F::kRingBytes);
   volatile uint32_t* abort_flag = &sh.abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,6 +210,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       mbar_init(smem_u32(&sh.a_local[s]), kDeqWarpsF);
       mbar_init(smem_u32(&sh.a_full[s]), 1);
       mbar_init(smem_u32(&sh.op_empty[s]), 1);
+      mbar_init(smem_u32(&sh.x_full[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sh.tmem_full[b]), 1);
@@ -208,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   auto mma_n = [&](int t) { return max(32, (min(kNTile, p.N - tile_n0(t)) + 15) & ~15); };
 
   if (warp == 0) {
-    // ===== TMA producer: packed X and W tiles =====
+    // ===== TMA producer: packed X and W tiles (BF16 X: packed W tiles only) =====
     if (lane == 0) {
       uint32_t uc = 0, pend_mask = 0, pend_par = 0;
       for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
@@ -226,8 +264,12 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           for (int h = 0; h < nk; ++h) {
             const int kb = kUnit * j + h;
             uint8_t* dst = ring_p + sl.idx * F::kUnitBytes + h * F::kStageBytes;
-            tma_load_2d(smem_u32(dst), &tm_x, full, kb * F::kRowBytes, m0);
-            tma_load_2d(smem_u32(dst + F::kTileBytes), &tm_w, full, kb * F::kRowBytes, wrow0);
+            if (XBF) {
+              tma_load_2d(smem_u32(dst), &tm_w, full, kb * F::kRowBytes, wrow0);
+            } else {
+              tma_load_2d(smem_u32(dst), &tm_x, full, kb * F::kRowBytes, m0);
+              tma_load_2d(smem_u32(dst + F::kTileBytes), &tm_w, full, kb * F::kRowBytes, wrow0);
+            }
           }
         }
         if (!ok) break;
@@ -283,7 +325,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         bool ok = true;
         for (int j = 0; j < units; ++j, ++uc) {
           const Slot sl = ring_slot<kOpStages>(uc);
-          if (!wait_phase(smem_u32(&sh.a_local[sl.idx]), sl.par, abort_flag, p.err, limit)) {
+          if (!wait_phase(smem_u32(&sh.a_local[sl.idx]), sl.par, abort_flag, p.err, limit) ||
+              (XBF && !wait_phase(smem_u32(&sh.x_full[sl.idx]), sl.par, abort_flag, p.err, limit))) {
             ok = false;
             break;
           }
@@ -292,6 +335,30 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
         if (!ok) break;
       }
+    }
+  } else if (warp == 3) {
+    // ===== BF16 X: TMA producer of the A ring (its own thread, so that the packed W tiles
+    // run ahead of the MMA independently) =====
+    if (XBF && lane == 0) {
+      uint32_t uc = 0, xpend_mask = 0, xpend_par = 0;
+      for (int t = cl_id; t < total_tiles && !*abort_flag; t += n_cl) {
+        const int m0 = tile_m0(t);
+        bool ok = true;
+        for (int j = 0; j < units; ++j, ++uc) {
+          // the A slot of this unit is free once the MMA that last read it has completed
+          const Slot so = ring_slot<kOpStages>(uc);
+          if (!wait_phase(smem_u32(&sh.op_empty[so.idx]), so.par ^ 1u, abort_flag, p.err, limit)) { ok = false; break; }
+          const int nk = min(kUnit, p.kblocks - kUnit * j);
+          const uint32_t xf = smem_u32(&sh.x_full[so.idx]);
+          mbar_arrive_expect_tx(xf, nk * kOpBytes);
+          xpend_mask |= 1u << so.idx;
+          xpend_par = (xpend_par & ~(1u << so.idx)) | (so.par << so.idx);
+          for (int h = 0; h < nk; ++h)
+            tma_load_2d(smem_u32(ring_a + so.idx * kOpUnitBytes + h * kOpBytes), &tm_x, xf, (kUnit * j + h) * kKb, m0);
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) drain_pending<kOpStages>(sh.x_full, xpend_mask, xpend_par, kDrainLimitNs);
     }
   } else if (warp >= 4 && warp < 8) {
     // ===== epilogue: lane = row of Y, 16 consecutive columns per TMEM load, 16-byte stores =====
@@ -343,6 +410,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     }
   } else if (warp >= kFirstDeqF) {
     // ===== dequantization: thread -> row r of the k-block, k half hk (32 k) =====
+    // (BF16 X: W's row only; its pairs are put back in natural k order, X's order)
     const int dq = warp - kFirstDeqF;
     const int team = dq / 8;
     const int tt = (dq % 8) * 32 + lane;         // 0..255 within the team
@@ -355,7 +423,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     const uint32_t p_off = r * F::kRowBytes + hk * (F::kRowBytes / 2);
     float xts = 0.f, wts = 0.f;
     if (FMT == BSQ_NVFP4) {
-      xts = __ldg(p.x_ts);
+      if (!XBF) xts = __ldg(p.x_ts);
       wts = __ldg(p.w_ts);
     }
     uint32_t uc = 0;
@@ -371,22 +439,23 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const Slot sp = ring_slot<F::kPUnits>(uc + j);
         const int k0 = kb * kKb + 32 * hk;
         const bool kok = present && k0 < p.K;
-        uint32_t xs, ws;
-        float xf, wf;
-        load_scale<FMT>(p.x_scale, p.x_scale_ld, p.x_shift, xrow, k0, kok && xok, xs, xf);
+        uint32_t xs = 0, ws;
+        float xf = 0.f, wf;
+        if (!XBF) load_scale<FMT>(p.x_scale, p.x_scale_ld, p.x_shift, xrow, k0, kok && xok, xs, xf);
         load_scale<FMT>(p.w_scale, p.w_scale_ld, p.w_shift, wrow, k0, kok && wok, ws, wf);
         ok = wait_phase(smem_u32(&sh.p_full[sp.idx]), sp.par, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint32_t pst = p_ring + sp.idx * F::kUnitBytes + team * F::kStageBytes;
         uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, wa = xa, wb = xa;
-        if (kok && xok) {
+        if (!XBF && kok && xok) {
           xa = lds128(pst + p_off);
           if (!F::kFp4) xb = lds128(pst + p_off + 16);
         }
+        const uint32_t pw = pst + (XBF ? 0 : F::kTileBytes) + p_off;
         if (kok && wok) {
-          wa = lds128(pst + F::kTileBytes + p_off);
-          if (!F::kFp4) wb = lds128(pst + F::kTileBytes + p_off + 16);
+          wa = lds128(pw);
+          if (!F::kFp4) wb = lds128(pw + 16);
         }
         // this lane's plain loads from the slot are performed before its TMA refill (see the
         // same release in bsq_gemm.cu)
@@ -394,15 +463,22 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.p_empty[sp.idx]));
         uint32_t v[4][4];
-        decode32<FMT>(xa, xb, xs, xf, xts, kok && xok, v);
+        if (XBF) {
+          decode32<FMT>(wa, wb, ws, wf, wts, kok && wok, v);
+          natural_order<FMT>(v);
+        } else {
+          decode32<FMT>(xa, xb, xs, xf, xts, kok && xok, v);
+        }
         ok = wait_phase(smem_u32(&sh.op_empty[sa.idx]), sa.par ^ 1u, abort_flag, p.err, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         if (present) {
-          const uint32_t at = a_ring + sa.idx * kOpUnitBytes + team * kOpBytes;
+          if (!XBF) {
+            const uint32_t at = a_ring + sa.idx * kOpUnitBytes + team * kOpBytes;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) sts128(at + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
-          decode32<FMT>(wa, wb, ws, wf, wts, kok && wok, v);
+            for (int jj = 0; jj < 4; ++jj) sts128(at + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
+            decode32<FMT>(wa, wb, ws, wf, wts, kok && wok, v);
+          }
           const uint32_t bt = b_ring + sa.idx * kOpUnitBytes + team * kOpBytes;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) sts128(bt + st_off[jj], v[jj][0], v[jj][1], v[jj][2], v[jj][3]);
@@ -444,12 +520,22 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   if (warp == 2) tmem_dealloc_pair(tmem_base, kTmemColsF);
 }
 
-template <int FMT>
+template <int FMT, bool XBF>
 int launch_forward_typed(const ForwardArgs& a, const char** msg) {
-  using F = FwdFmt<FMT>;
+  using F = FwdFmt<FMT, XBF>;
   CUtensorMap tm_x, tm_w;
   const uint64_t row_bytes = FMT == BSQ_FP8_E4M3_B128 ? a.K : a.K / 2;
-  {
+  if (XBF) {
+    // BF16 X [M][K]: 64 k x 128 rows per box, 128-byte swizzled (the A operand's K-major layout)
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
+    const uint32_t box[2] = {static_cast<uint32_t>(kKb), static_cast<uint32_t>(kRowsF)};
+    if (!encode_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x_data, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B)) {
+      *msg = "tensor map encoding failed for X";
+      return -1;
+    }
+  } else {
     const uint64_t dims[2] = {row_bytes, static_cast<uint64_t>(a.M)};
     const uint64_t strides[1] = {row_bytes};
     const uint32_t box[2] = {static_cast<uint32_t>(F::kRowBytes), static_cast<uint32_t>(kRowsF)};
@@ -493,7 +579,7 @@ int launch_forward_typed(const ForwardArgs& a, const char** msg) {
   p.timeout_ns = wait_limit_ns();
   static_assert(F::kRingBytes + sizeof(FwdShared) + 1024 <= 232448, "rings exceed the shared memory of a CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(FwdShared) + 1024;
-  auto kern = bsq_forward_kernel<FMT>;
+  auto kern = bsq_forward_kernel<FMT, XBF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -534,11 +620,20 @@ int launch_forward_typed(const ForwardArgs& a, const char** msg) {
 }  // namespace
 
 int launch_forward(const ForwardArgs& a, const char** msg) {
-  switch (kernel_fmt(a.x_fmt)) {
-    case BSQ_FP8_E4M3_B128: return launch_forward_typed<BSQ_FP8_E4M3_B128>(a, msg);
-    case BSQ_MXFP4: return launch_forward_typed<BSQ_MXFP4>(a, msg);
-    case BSQ_NVFP4: return launch_forward_typed<BSQ_NVFP4>(a, msg);
-    default: break;
+  if (a.x_fmt == BSQ_BF16) {
+    switch (kernel_fmt(a.w_fmt)) {
+      case BSQ_FP8_E4M3_B128: return launch_forward_typed<BSQ_FP8_E4M3_B128, true>(a, msg);
+      case BSQ_MXFP4: return launch_forward_typed<BSQ_MXFP4, true>(a, msg);
+      case BSQ_NVFP4: return launch_forward_typed<BSQ_NVFP4, true>(a, msg);
+      default: break;
+    }
+  } else {
+    switch (kernel_fmt(a.x_fmt)) {
+      case BSQ_FP8_E4M3_B128: return launch_forward_typed<BSQ_FP8_E4M3_B128, false>(a, msg);
+      case BSQ_MXFP4: return launch_forward_typed<BSQ_MXFP4, false>(a, msg);
+      case BSQ_NVFP4: return launch_forward_typed<BSQ_NVFP4, false>(a, msg);
+      default: break;
+    }
   }
   *msg = "forward: unsupported format";
   return -1;

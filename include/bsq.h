@@ -172,8 +172,10 @@ bsq_status bsq_linear_backward(const void* grad_out, int64_t M, int64_t N,
  * multiply packed X and W; the backward the PR adds is that of this product).  Both
  * operands are dequantized with the rule above, multiplied on the tensor cores with FP32
  * accumulation and rounded once to BF16.
- * X: packed [1][M][K] in x_fmt, W: packed [1][N][K] in w_fmt; both packed (not BSQ_BF16) and
- * of one kind: both FP4 of one format, or both FP8 (128x128 blocks or per tensor, mixed).
+ * X: packed [1][M][K] in x_fmt, W: packed [1][N][K] in w_fmt; W packed (not BSQ_BF16).  X is
+ * either BSQ_BF16 (a BF16 activation, as in the FP8 linear layer of transformers PR #50031
+ * whose weight alone is quantized: y = X @ deq(W)^T, K % 8 == 0) or packed of the same kind
+ * as W: both FP4 of one format, or both FP8 (128x128 blocks or per tensor, mixed).
  * y: bf16[M][N], fully written; N % 8 == 0.  K == 0 gives zeros.
  */
 bsq_status bsq_linear_forward(int32_t x_fmt, const void* x_data, const void* x_scale,

@@ -97,7 +97,11 @@ def test_fp8_per_tensor_format_validation(L):
 def test_linear_forward_validation(L):
     def fw(xf=2, wf=2, M=64, N=128, K=256, y=FAKE):
         return L.bsq_linear_forward(xf, FAKE, FAKE, FAKE, M, wf, FAKE, FAKE, FAKE, N, K, y, None)
-    assert fw(xf=0) == bsq.BSQ_ERR_UNSUPPORTED          # BF16 X is not a packed operand
+    assert fw(wf=0) == bsq.BSQ_ERR_UNSUPPORTED          # the weight is packed
+    assert fw(xf=0, wf=0) == bsq.BSQ_ERR_UNSUPPORTED
+    assert fw(xf=0, K=100) == bsq.BSQ_ERR_UNSUPPORTED   # BF16 X row pitch: K % 8
+    assert fw(xf=0, wf=3, K=48) == bsq.BSQ_ERR_UNSUPPORTED   # NVFP4 W: K % 32
+    assert fw(xf=0, M=0) == bsq.BSQ_OK                  # BF16 X with a packed W: accepted
     assert fw(xf=2, wf=3) == bsq.BSQ_ERR_UNSUPPORTED    # MXFP4 x NVFP4: no common kernel
     assert fw(N=12) == bsq.BSQ_ERR_UNSUPPORTED          # Y row pitch
     assert fw(y=None) == bsq.BSQ_ERR_INVALID_ARG

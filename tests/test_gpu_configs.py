@@ -5,8 +5,9 @@ four columns of every 128-column block (each block is one m-tile of the GEMM ker
 a wrong block of any CTA is seen): the oracle dequantizes only those columns of the
 packed operand and forms the float64 products, so every expert-boundary row is covered.
 Rows past offsets[E-1] (none here: all five workloads route every token) and empty
-experts are checked exactly.  The forward on the two dense workloads and the E5M2
-backward on the MXFP4 4096^3 one are checked the same way.
+experts are checked exactly.  The forward on the two dense workloads (packed X, and a BF16
+X as in the FP8 linear layer, whose own forward is checked whole) and the E5M2 backward on
+the MXFP4 4096^3 one are checked the same way.
 """
 
 import pytest
@@ -65,6 +66,31 @@ def test_forward_full_size_sampled(n):
     x = oracle_deq(c["X"])[0]
     got = bf16_vals(y[:, torch.from_numpy(cols).cuda()])
     assert_gemm(got, Gm.forward(x, w), x, w, c["K"], f"{c['name']} forward")
+    st, code = bsq.get_device_error()
+    assert st == bsq.BSQ_OK and code == 0
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_forward_bf16_activation_full_size(n):
+    """bsq_linear_forward with a BF16 X and a packed W: the FP8 linear workload's own layer
+    (its X is BF16) compared on every element, and the two dense workloads' weights against
+    a seeded BF16 activation of their X's shape and law, every row on four columns of every
+    128-column block."""
+    c = synth.make_config(n, device="cuda")
+    if n == 1:
+        X = c["X"]
+    else:
+        X = synth.make_packed(synth.FMT_BF16, 1, c["X"].rows, c["K"], {2: 1.0, 3: 0.02}[n], 150 + n, "cuda")
+    assert X.fmt == synth.FMT_BF16
+    y = bsq.linear_forward(X, c["W"])
+    torch.cuda.synchronize()
+    W = c["W"]
+    cols = np.arange(c["N"]) if n == 1 else _cols(c["N"], 126)
+    d, sc, ts = W.numpy()
+    w = D.dequant_rows(ORACLE_FMT[W.fmt], d, sc, ts, W.rows, W.cols, cols)
+    x = oracle_deq(X)[0]
+    got = bf16_vals(y[:, torch.from_numpy(cols).cuda()])
+    assert_gemm(got, Gm.forward(x, w), x, w, c["K"], f"{c['name']} forward, BF16 X")
     st, code = bsq.get_device_error()
     assert st == bsq.BSQ_OK and code == 0
 
