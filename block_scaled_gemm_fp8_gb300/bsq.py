@@ -214,7 +214,7 @@ def linear_backward_e5m2(grad_out, w, x, needs=BSQ_NEEDS_GRAD_X | BSQ_NEEDS_GRAD
 
 
 def linear_forward(x, w, out=None, stream=None):
-    """y[M,N] = deq(X)[M,K] @ deq(W)[N,K]^T with both operands packed."""
+    """y[M,N] = deq(X)[M,K] @ deq(W)[N,K]^T; W packed, X packed of W's kind or BF16 (fmt 0)."""
     if out is None:
         out = torch.empty((x.rows, w.rows), dtype=torch.bfloat16, device=x.data.device)
     _check(lib().bsq_linear_forward(x.fmt, _ptr(x.data), _ptr(x.scale), _ptr(x.tensor_scale), x.rows, w.fmt,
