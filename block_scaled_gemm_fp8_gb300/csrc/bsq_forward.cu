@@ -95,6 +95,7 @@ struct FwdParams {
   int32_t x_scale_ld, w_scale_ld;      // scale row pitch (elements)
   int32_t x_shift, w_shift;            // FP8: log2 of the scale block's side (7, or 31 per tensor)
   uint64_t timeout_ns;
+  int32_t drop_announce;       // test hook: the even CTA's relay never announces a unit
 };
 
 struct FwdShared {
@@ -330,8 +331,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(a_full0 + 8 * sl.idx, 4);
-          else st_async_tx_rank(smem_u32(&sh.sink), a_full0 + 8 * sl.idx, 0);
+          if (rank == 0) {
+            if (!p.drop_announce) mbar_arrive_expect_tx(a_full0 + 8 * sl.idx, 4);
+          } else {
+            st_async_tx_rank(smem_u32(&sh.sink), a_full0 + 8 * sl.idx, 0);
+          }
         }
         if (!ok) break;
       }
@@ -577,6 +581,11 @@ int launch_forward_typed(const ForwardArgs& a, const char** msg) {
   p.x_shift = fp8_scale_shift(a.x_fmt);
   p.w_shift = fp8_scale_shift(a.w_fmt);
   p.timeout_ns = wait_limit_ns();
+  // Test hook (failure detection without a GPU fault): with BSQ_TEST_DROP_ANNOUNCE=1 the even
+  // CTA's relay withholds its operand-ready arrivals, so the MMA thread's first wait runs out
+  // and the kernel takes its orderly abort.
+  const char* drop = std::getenv("BSQ_TEST_DROP_ANNOUNCE");
+  p.drop_announce = drop && drop[0] == '1' ? 1 : 0;
   static_assert(F::kRingBytes + sizeof(FwdShared) + 1024 <= 232448, "rings exceed the shared memory of a CTA");
   const size_t smem = static_cast<size_t>(F::kRingBytes) + sizeof(FwdShared) + 1024;
   auto kern = bsq_forward_kernel<FMT, XBF>;

@@ -1,4 +1,4 @@
-"""Failure detection without a GPU fault: a pipeline wait of the GEMM kernel runs out.
+"""Failure detection without a GPU fault: a pipeline wait of the GEMM or forward kernel runs out.
 
 Every wait inside the kernels is bounded (BSQ_WAIT_LIMIT_MS / _US); on expiry the kernel
 lets its copies in flight land, stops every role of both CTAs of the pair, frees its
@@ -7,9 +7,10 @@ the test hook BSQ_TEST_DROP_ANNOUNCE=1 withholds the even CTA's operand-ready
 announcements (a flag nothing sets), so the MMA thread's first wait runs out after a
 50 ms limit.  The test checks that bsq_get_device_error reports BSQ_ERR_TIMEOUT, and that
 the next calls in the same process, with the hook off, are correct and leave no error.
-It covers the default kernel (linear dgrad), the short-tile kernel (grouped wgrad) and the
-fused backward launch, and runs in a child process so that its environment settings touch
-no other test.
+It covers the default kernel (linear dgrad), the short-tile kernel (grouped wgrad), the
+fused backward launch and the forward kernel (packed X, and BF16 X with its own X
+producer), and runs in a child process so that its environment settings touch no other
+test.
 """
 
 import os
@@ -38,10 +39,14 @@ SCRIPT = textwrap.dedent("""
     wd, xd, gd = W.to("cuda"), X.to("cuda"), G.cuda()
     offs = synth.offsets_from_counts([100, 0, 200])
     od = torch.from_numpy(offs).cuda()
+    XB = synth.make_packed(synth.FMT_BF16, 1, 300, 512, 1.0, seed=4, device="cpu")
+    xbd = XB.to("cuda")
     calls = {{
         "linear_dgrad": lambda: bsq.linear_dgrad(gd, wd),
         "grouped_wgrad": lambda: bsq.grouped_wgrad(gd, xd, od, 3),
         "linear_backward": lambda: bsq.linear_backward(gd, wd, xd),
+        "linear_forward": lambda: bsq.linear_forward(xd, wd),
+        "linear_forward_bf16_x": lambda: bsq.linear_forward(xbd, wd),
     }}
     g, w, x = bf16_vals(G), oracle_deq(W)[0], oracle_deq(X)[0]
     for name, call in calls.items():
@@ -64,6 +69,11 @@ SCRIPT = textwrap.dedent("""
                     assert_gemm(got[e], ref[e], g[r0:r1], x[r0:r1], r1 - r0, f"{{name}} e={{e}}")
                 else:
                     assert (got[e] == 0).all()
+        elif name == "linear_forward":
+            assert_gemm(bf16_vals(out), Gm.forward(x, w), x, w, 512, name)
+        elif name == "linear_forward_bf16_x":
+            xb = oracle_deq(XB)[0]
+            assert_gemm(bf16_vals(out), Gm.forward(xb, w), xb, w, 512, name)
         else:
             gx, gw = out
             assert_gemm(bf16_vals(gx), Gm.dgrad(g, w), g, w, 256, name + " dgrad")
@@ -79,4 +89,4 @@ def test_wait_runs_out_then_next_call_is_correct():
     r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert r.stdout.count("ok ") == 3, r.stdout
+    assert r.stdout.count("ok ") == 5, r.stdout
