@@ -69,11 +69,11 @@
  *       BSQ_GROUPED_TAIL_ROWS above that bound, an expert's ragged last GEMM tile of at most
  *                             this many rows (0..255, default 0 = none) goes to the small-M
  *                             kernel instead; the two kernels then run one after the other.
- *       BSQ_TEST_DROP_ANNOUNCE test hook for failure detection: 1 = in the GEMM kernels, the
- *                             even CTA of each pair never announces a unit's operands, so the
+ *       BSQ_TEST_DROP_ANNOUNCE test hook for failure detection: 1 = in the GEMM and forward
+ *                             kernels, the even CTA of each pair never announces a unit's operands, so the
  *                             MMA thread's wait runs out of time (BSQ_WAIT_LIMIT_*), the kernel
  *                             stops in order and records BSQ_DEVERR_TIMEOUT.  Never set it
- *                             outside such a test: every GEMM call then fails.
+ *                             outside such a test: every GEMM and forward call then fails.
  *       BSQ_TEST_DROP_CHUNK   the same for the small-M kernel (bsq_linear_dgrad with M <= 16,
  *                             decode-sized bsq_grouped_dgrad): every CTA's first chunk is
  *                             never requested, so the wait for it runs out.
