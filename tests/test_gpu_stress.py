@@ -18,6 +18,9 @@ that the kernels' loads meet a busy memory system at varying moments.  A result 
 depends on when a load completes relative to the refill of its buffer (a ring slot read
 with plain loads and refilled by TMA without an order between the two) differs from the
 clean run there.
+
+A third test repeats the forward kernel (same pair protocol) with a packed X and with a
+BF16 X, half of the repeats under the same concurrent copies.
 """
 
 import pytest
@@ -89,3 +92,46 @@ def test_repeats_under_concurrent_memory_traffic_match_first_run(n):
     st, code = bsq.get_device_error()
     assert st == bsq.BSQ_OK and code == 0, (st, code)
     assert not bad, f"{c['name']}: repeats under concurrent traffic that differ from the clean run: {bad}"
+
+
+@pytest.mark.parametrize("x_bf16", [False, True])
+def test_forward_repeats_match_oracle_and_first_run(x_bf16):
+    """The forward kernel's pair protocol, repeated: Y = X W^T on the MXFP4 4096^3 workload's
+    W with its packed X or a BF16 X (TMA into the A ring, its own producer warp), the first
+    run against the oracle on four columns of every 128-column block, then REPS runs into
+    NaN-filled buffers, every other one while another stream copies 2 GB buffers; each must
+    equal the first bit for bit."""
+    from oracle import dequant as D
+    from oracle import gemm as Gm
+    from tests._util import ORACLE_FMT, assert_gemm, bf16_vals, oracle_deq
+    c = synth.make_config(2, device="cuda")
+    X = synth.make_packed(synth.FMT_BF16, 1, c["M"], c["K"], 1.0, 160, "cuda") if x_bf16 else c["X"]
+    y = bsq.linear_forward(X, c["W"])
+    torch.cuda.synchronize()
+    cols = block_cols(c["N"], 4, 161)
+    W = c["W"]
+    d, sc, ts = W.numpy()
+    w = D.dequant_rows(ORACLE_FMT[W.fmt], d, sc, ts, W.rows, W.cols, cols)
+    x = oracle_deq(X)[0]
+    assert_gemm(bf16_vals(y[:, torch.from_numpy(cols).cuda()]), Gm.forward(x, w), x, w, c["K"],
+                f"forward bf16_x={x_bf16}")
+    ref = y.clone()
+    src = torch.empty(1 << 31, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    side = torch.cuda.Stream()
+    bad = []
+    for rep in range(REPS):
+        y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        if rep % 2:
+            with torch.cuda.stream(side):
+                dst.copy_(src)
+            torch.cuda._sleep(10000 * (rep % 5))
+        bsq.linear_forward(X, c["W"], out=y)
+        if not torch.equal(y.view(torch.int16), ref.view(torch.int16)):
+            bad.append((rep, int((y.view(torch.int16) != ref.view(torch.int16)).sum().item())))
+    torch.cuda.synchronize()
+    del src, dst
+    st, code = bsq.get_device_error()
+    assert st == bsq.BSQ_OK and code == 0, (st, code)
+    assert not bad, f"forward bf16_x={x_bf16}: repeats that differ from the first run (rep, elements): {bad}"
